@@ -1,0 +1,239 @@
+// C-ABI entry points of libsparse_paged_kv (declared in include/locks.h):
+// argument validation, workspace sizing and kernel dispatch.  Nothing here
+// allocates, frees or synchronises.
+#include <cmath>
+#include <cstdint>
+
+#include "locks_common.cuh"
+#include "locks_internal.h"
+
+namespace {
+
+using locks::kHeadDim;
+using locks::kPageSize;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool is_pow2_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+int check_cfg(const locks_cfg_t* c) {
+  if (!c) return LOCKS_ERR_INVALID_ARG;
+  if (c->batch < 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->max_pages <= 0 ||
+      c->num_blocks <= 0 || c->rank <= 0 || c->head_dim <= 0 || c->page_size <= 0)
+    return LOCKS_ERR_INVALID_ARG;
+  if (c->n_q_heads % c->n_kv_heads != 0) return LOCKS_ERR_INVALID_ARG;
+  if (c->summary_dtype != LOCKS_SUMMARY_F32 && c->summary_dtype != LOCKS_SUMMARY_BF16)
+    return LOCKS_ERR_INVALID_ARG;
+  if (c->head_dim != kHeadDim || c->page_size != kPageSize) return LOCKS_ERR_UNSUPPORTED;
+  if (c->rank > 16) return LOCKS_ERR_UNSUPPORTED;
+  if (!is_pow2_group(c->n_q_heads / c->n_kv_heads)) return LOCKS_ERR_UNSUPPORTED;
+  return LOCKS_OK;
+}
+
+int group_of(const locks_cfg_t* c) { return c->n_q_heads / c->n_kv_heads; }
+
+size_t elem_bytes(const locks_cfg_t* c) { return c->summary_dtype == LOCKS_SUMMARY_F32 ? 4 : 2; }
+
+int page_budget(int budget_tokens, int page_size) {
+  return (budget_tokens + page_size - 1) / page_size;   // k = ceil(b / B)
+}
+
+// ---- select workspace -------------------------------------------------------
+struct SelectLayout {
+  size_t scores, part, ticket, total;
+  int chunk_pages, n_chunks_max;
+};
+
+SelectLayout select_layout(const locks_cfg_t* c) {
+  SelectLayout L;
+  const int G = group_of(c);
+  const size_t U = size_t(c->batch) * c->n_kv_heads;
+  L.chunk_pages = locks::select_chunk_pages(c->max_pages);
+  const int max_cand = c->max_pages > 2 ? c->max_pages - 2 : 0;
+  L.n_chunks_max = max_cand > 0 ? (max_cand + L.chunk_pages - 1) / L.chunk_pages : 1;
+  L.scores = 0;
+  L.part = L.scores + align_up(U * c->max_pages * G * sizeof(float));
+  L.ticket = L.part + align_up(U * L.n_chunks_max * G * sizeof(float2));
+  L.total = L.ticket + align_up(U * sizeof(int32_t));
+  return L;
+}
+
+// ---- decode workspace -------------------------------------------------------
+struct DecodeLayout {
+  size_t part, ticket, total;
+  int pages_per_split, n_splits_max;
+};
+
+DecodeLayout decode_layout(const locks_cfg_t* c, int n_pages) {
+  DecodeLayout L;
+  const int G = group_of(c);
+  const size_t U = size_t(c->batch) * c->n_kv_heads;
+  // aim for about three waves of two CTAs per SM on 152 SMs
+  const double total_pages = double(U) * (n_pages > 0 ? n_pages : 1);
+  int pps = int(std::ceil(total_pages / (152.0 * 2.0 * 3.0)));
+  if (pps < 1) pps = 1;
+  if (pps > 64) pps = 64;
+  L.pages_per_split = pps;
+  L.n_splits_max = n_pages > 0 ? (n_pages + pps - 1) / pps : 1;
+  L.part = 0;
+  L.ticket = align_up(U * L.n_splits_max * G * locks::kPartStride * sizeof(float));
+  L.total = L.ticket + align_up(U * sizeof(int32_t));
+  return L;
+}
+
+int decode_common(const locks_cfg_t* cfg, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_table, const int32_t* seq_lens, const int32_t* selected,
+                  int32_t k, int n_list_max, void* out, float* out_lse, void* workspace,
+                  size_t workspace_bytes, int32_t* status, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc != LOCKS_OK) return rc;
+  if (cfg->batch == 0) return LOCKS_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace)
+    return LOCKS_ERR_INVALID_ARG;
+  const DecodeLayout L = decode_layout(cfg, n_list_max);
+  if (workspace_bytes < L.total) return LOCKS_ERR_WORKSPACE;
+  locks::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  p.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.selected = selected;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out_lse = out_lse;
+  p.status = status;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.ws_part = reinterpret_cast<float*>(ws + L.part);
+  p.ws_ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
+  p.n_kv_heads = cfg->n_kv_heads;
+  p.max_pages = cfg->max_pages;
+  p.num_blocks = cfg->num_blocks;
+  p.k = k;
+  p.pages_per_split = L.pages_per_split;
+  p.n_splits_max = L.n_splits_max;
+  p.scale = float(1.0 / std::sqrt(double(cfg->head_dim)));
+  p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(cfg->head_dim)));
+  const int U = cfg->batch * cfg->n_kv_heads;
+  return locks::launch_decode(p, group_of(cfg), L.n_splits_max, U,
+                              static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t locks_summary_record_bytes(const locks_cfg_t* cfg) {
+  if (check_cfg(cfg) != LOCKS_OK) return 0;
+  const int rp = locks::rank_cap(cfg->rank);
+  return size_t(locks::rec_elems(rp, cfg->page_size)) * elem_bytes(cfg);
+}
+
+size_t locks_select_workspace_bytes(const locks_cfg_t* cfg, int32_t budget_tokens) {
+  (void)budget_tokens;
+  if (check_cfg(cfg) != LOCKS_OK) return 0;
+  return select_layout(cfg).total;
+}
+
+size_t locks_decode_workspace_bytes(const locks_cfg_t* cfg, int32_t n_pages) {
+  if (check_cfg(cfg) != LOCKS_OK || n_pages < 0) return 0;
+  return decode_layout(cfg, n_pages).total;
+}
+
+int locks_build_summaries(const locks_cfg_t* cfg, const void* k_cache, const int32_t* block_ids,
+                          int32_t n_blocks, void* summaries, float* tail_energy, int32_t* status,
+                          int32_t max_sweeps, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc != LOCKS_OK) return rc;
+  if (n_blocks < 0 || max_sweeps < 0) return LOCKS_ERR_INVALID_ARG;
+  if (n_blocks == 0) return LOCKS_OK;
+  if (!k_cache || !block_ids || !summaries) return LOCKS_ERR_INVALID_ARG;
+  locks::BuildParams p;
+  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  p.block_ids = block_ids;
+  p.summaries = summaries;
+  p.tail_energy = tail_energy;
+  p.status = status;
+  p.rec_bytes = locks_summary_record_bytes(cfg);
+  p.n_blocks = n_blocks;
+  p.n_kv_heads = cfg->n_kv_heads;
+  p.num_blocks = cfg->num_blocks;
+  p.rank = cfg->rank;
+  p.max_sweeps = max_sweeps == 0 ? 20 : max_sweeps;
+  return locks::launch_build(p, locks::rank_cap(cfg->rank), cfg->summary_dtype,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int locks_select(const locks_cfg_t* cfg, const void* q, const void* summaries,
+                 const int32_t* block_table, const int32_t* seq_lens, int32_t budget_tokens,
+                 int32_t* selected, float* page_lse, float* page_share, void* workspace,
+                 size_t workspace_bytes, int32_t* status, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc != LOCKS_OK) return rc;
+  const int k = page_budget(budget_tokens, cfg->page_size);
+  if (budget_tokens <= 0 || k < 2) return LOCKS_ERR_INVALID_ARG;
+  if (k > 256) return LOCKS_ERR_UNSUPPORTED;
+  if (cfg->batch == 0) return LOCKS_OK;
+  if (!q || !summaries || !block_table || !seq_lens || !selected || !workspace)
+    return LOCKS_ERR_INVALID_ARG;
+  const SelectLayout L = select_layout(cfg);
+  if (workspace_bytes < L.total) return LOCKS_ERR_WORKSPACE;
+  locks::SelectParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.summaries = summaries;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.selected = selected;
+  p.page_lse = page_lse;
+  p.page_share = page_share;
+  p.status = status;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.ws_scores = reinterpret_cast<float*>(ws + L.scores);
+  p.ws_part = reinterpret_cast<float2*>(ws + L.part);
+  p.ws_ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
+  p.rec_bytes = locks_summary_record_bytes(cfg);
+  p.n_kv_heads = cfg->n_kv_heads;
+  p.max_pages = cfg->max_pages;
+  p.num_blocks = cfg->num_blocks;
+  p.k = k;
+  p.chunk_pages = L.chunk_pages;
+  p.n_chunks_max = L.n_chunks_max;
+  p.scale = float(1.0 / std::sqrt(double(cfg->head_dim)));
+  p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(cfg->head_dim)));
+  const int U = cfg->batch * cfg->n_kv_heads;
+  return locks::launch_select(p, group_of(cfg), locks::rank_cap(cfg->rank), cfg->summary_dtype,
+                              L.n_chunks_max, U, static_cast<cudaStream_t>(stream));
+}
+
+int locks_sparse_decode(const locks_cfg_t* cfg, const void* q, const void* k_cache,
+                        const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                        const int32_t* selected, int32_t k, void* out, float* out_lse,
+                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  if (!cfg || !selected || k <= 0) return LOCKS_ERR_INVALID_ARG;
+  return decode_common(cfg, q, k_cache, v_cache, block_table, seq_lens, selected, k, k, out,
+                       out_lse, workspace, workspace_bytes, status, stream);
+}
+
+int locks_dense_decode(const locks_cfg_t* cfg, const void* q, const void* k_cache,
+                       const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                       void* out, float* out_lse, void* workspace, size_t workspace_bytes,
+                       int32_t* status, void* stream) {
+  if (!cfg) return LOCKS_ERR_INVALID_ARG;
+  return decode_common(cfg, q, k_cache, v_cache, block_table, seq_lens, nullptr, 0,
+                       cfg->max_pages, out, out_lse, workspace, workspace_bytes, status, stream);
+}
+
+const char* locks_status_string(int code) {
+  switch (code) {
+    case LOCKS_OK: return "ok";
+    case LOCKS_ERR_INVALID_ARG: return "invalid argument";
+    case LOCKS_ERR_UNSUPPORTED: return "unsupported shape";
+    case LOCKS_ERR_WORKSPACE: return "workspace too small";
+    case LOCKS_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+int locks_abi_version(void) { return LOCKS_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,293 @@
+// locks_build_summaries: the per-page spectral key summary of
+// "Locks: Page-Local Compact Key Summaries for Efficient Long-Context
+// Decoding", section 4 "Build" (and the blog review's Algorithm 1).
+//
+// One CTA of 256 threads per (block, KV head) page:
+//   1. load the page's B = 64 bf16 keys, mu = mean of the keys, D = K - mu (fp32);
+//   2. Gram A = D D^T (64 x 64), 4 x 4 register tiles per thread;
+//   3. parallel cyclic Jacobi: each sweep is 63 rounds of 32 disjoint
+//      (p, q) rotations (round-robin ordering, so every pair meets once per
+//      sweep); a round applies A <- J^T A J as 1024 independent 2 x 2 block
+//      transforms and U <- U J; sweeps stop when the off-diagonal Frobenius
+//      norm falls below 1e-6 of the total (or at max_sweeps, flagged);
+//   4. the top-r eigenpairs in descending order (ties: lower index); modes
+//      with sigma^2 <= 1e-5 sigma_1^2 are dropped (zero basis column and
+//      coefficients); V = D^T U_r S_r^-1, C = U_r S_r,
+//      tau = sum of the remaining eigenvalues;
+//   5. the record (mu, V, C) in the layout locks_select reads.
+#include "locks_common.cuh"
+#include "locks_internal.h"
+
+namespace locks {
+
+namespace {
+
+constexpr int kBuildThreads = 256;
+constexpr int kDS = kHeadDim + 4;   // padded row stride of D (floats)
+constexpr int kAS = kPageSize + 1;  // padded row stride of A and U
+constexpr float kJacobiTol = 1e-6f;
+constexpr float kDropRel = 1e-5f;
+
+struct BuildSmem {
+  float D[kPageSize * kDS];
+  float A[kPageSize * kAS];
+  float U[kPageSize * kAS];
+  float mu[kHeadDim];
+  float rot_c[32], rot_s[32];
+  int rot_p[32], rot_q[32];
+  float red[kBuildThreads / 32 * 2];
+  float lam[16];
+  int order[16];
+  float tau;
+  int flag;
+};
+
+__device__ __forceinline__ void round_pair(int t, int k, int& p, int& q) {
+  // circle method on 64 players: player 63 fixed, the other 63 rotate
+  int a, b;
+  if (k == 0) { a = t; b = kPageSize - 1; }
+  else { a = (t + k) % (kPageSize - 1); b = (t - k + (kPageSize - 1)) % (kPageSize - 1); }
+  p = min(a, b);
+  q = max(a, b);
+}
+
+template <int RP, typename T>
+__global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams prm) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  BuildSmem& S = *reinterpret_cast<BuildSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int pid = blockIdx.x;
+  const int h = blockIdx.y;
+  const int out_idx = pid * prm.n_kv_heads + h;
+  const int blk = prm.block_ids[pid];
+  if (blk < 0 || blk >= prm.num_blocks) {
+    if (tid == 0 && prm.status) prm.status[out_idx] = LOCKS_DEV_BAD_BLOCK_ID << 16;
+    return;
+  }
+
+  // ---- 1. keys -> D, mu ----------------------------------------------------
+  const uint4* src = reinterpret_cast<const uint4*>(
+      prm.k_cache + (size_t(blk) * prm.n_kv_heads + h) * (kPageSize * kHeadDim));
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int idx = tid + kBuildThreads * e;       // 16-byte chunk of the 16 KiB page
+    const int row = idx >> 4, col = (idx & 15) * 8;
+    const uint4 w = src[idx];
+    float* d = S.D + row * kDS + col;
+    d[0] = bf16_lo(w.x); d[1] = bf16_hi(w.x); d[2] = bf16_lo(w.y); d[3] = bf16_hi(w.y);
+    d[4] = bf16_lo(w.z); d[5] = bf16_hi(w.z); d[6] = bf16_lo(w.w); d[7] = bf16_hi(w.w);
+  }
+  __syncthreads();
+  if (tid < kHeadDim) {
+    float s = 0.f;
+    for (int i = 0; i < kPageSize; ++i) s += S.D[i * kDS + tid];
+    S.mu[tid] = s * (1.f / kPageSize);
+  }
+  __syncthreads();
+  for (int idx = tid; idx < kPageSize * kHeadDim; idx += kBuildThreads) {
+    const int i = idx >> 7, t = idx & 127;
+    S.D[i * kDS + t] -= S.mu[t];
+  }
+  __syncthreads();
+
+  // ---- 2. Gram A = D D^T: thread (ti, tj) owns rows ti+16a, cols tj+16b ----
+  {
+    const int ti = tid >> 4, tj = tid & 15;
+    float acc[4][4] = {};
+    for (int c = 0; c < kHeadDim; c += 4) {
+      float4 di[4], dj[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        di[a] = *reinterpret_cast<const float4*>(S.D + (ti + 16 * a) * kDS + c);
+        dj[a] = *reinterpret_cast<const float4*>(S.D + (tj + 16 * a) * kDS + c);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb)
+          acc[a][bb] += di[a].x * dj[bb].x + di[a].y * dj[bb].y + di[a].z * dj[bb].z +
+                        di[a].w * dj[bb].w;
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) S.A[(ti + 16 * a) * kAS + tj + 16 * bb] = acc[a][bb];
+  }
+  for (int idx = tid; idx < kPageSize * kPageSize; idx += kBuildThreads) {
+    const int i = idx >> 6, j = idx & 63;
+    S.U[i * kAS + j] = (i == j) ? 1.f : 0.f;
+  }
+  __syncthreads();
+
+  // ---- 3. Jacobi sweeps ------------------------------------------------------
+  int sweeps = 0;
+  bool converged = false;
+  for (;;) {
+    // off-diagonal and total Frobenius norms
+    float off = 0.f, tot = 0.f;
+    for (int idx = tid; idx < kPageSize * kPageSize; idx += kBuildThreads) {
+      const int i = idx >> 6, j = idx & 63;
+      const float a = S.A[i * kAS + j];
+      tot += a * a;
+      if (i != j) off += a * a;
+    }
+    off = group_sum<32>(off);
+    tot = group_sum<32>(tot);
+    if (lane == 0) { S.red[2 * warp] = off; S.red[2 * warp + 1] = tot; }
+    __syncthreads();
+    if (tid == 0) {
+      float o = 0.f, t = 0.f;
+      for (int w = 0; w < kBuildThreads / 32; ++w) { o += S.red[2 * w]; t += S.red[2 * w + 1]; }
+      S.flag = (o <= kJacobiTol * kJacobiTol * t) ? 1 : 0;
+    }
+    __syncthreads();
+    if (S.flag) { converged = true; break; }
+    if (sweeps >= prm.max_sweeps) break;
+    ++sweeps;
+    for (int r = 0; r < kPageSize - 1; ++r) {
+      if (tid < 32) {
+        int p, q;
+        round_pair(r, tid, p, q);
+        const float app = S.A[p * kAS + p], aqq = S.A[q * kAS + q], apq = S.A[p * kAS + q];
+        float c = 1.f, s = 0.f;
+        if (apq != 0.f) {
+          const float theta = (aqq - app) / (2.f * apq);
+          float t;
+          if (fabsf(theta) > 1e18f) t = 0.5f / theta;
+          else t = (theta >= 0.f ? 1.f : -1.f) / (fabsf(theta) + sqrtf(1.f + theta * theta));
+          c = rsqrtf(1.f + t * t);
+          s = t * c;
+        }
+        S.rot_c[tid] = c; S.rot_s[tid] = s; S.rot_p[tid] = p; S.rot_q[tid] = q;
+      }
+      __syncthreads();
+      {
+        // 2 x 2 blocks (K, L): rows (pK, qK), cols (pL, qL); B'' = J_K^T B J_L
+        const int K = tid >> 3;
+        const float cK = S.rot_c[K], sK = S.rot_s[K];
+        const int pK = S.rot_p[K], qK = S.rot_q[K];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int L = (tid & 7) + 8 * m;
+          const float cL = S.rot_c[L], sL = S.rot_s[L];
+          const int pL = S.rot_p[L], qL = S.rot_q[L];
+          float* a00 = S.A + pK * kAS + pL;
+          float* a01 = S.A + pK * kAS + qL;
+          float* a10 = S.A + qK * kAS + pL;
+          float* a11 = S.A + qK * kAS + qL;
+          const float b00 = *a00, b01 = *a01, b10 = *a10, b11 = *a11;
+          const float x00 = cK * b00 - sK * b10, x01 = cK * b01 - sK * b11;
+          const float x10 = sK * b00 + cK * b10, x11 = sK * b01 + cK * b11;
+          float n00 = x00 * cL - x01 * sL, n01 = x00 * sL + x01 * cL;
+          float n10 = x10 * cL - x11 * sL, n11 = x10 * sL + x11 * cL;
+          if (K == L) { n01 = 0.f; n10 = 0.f; }
+          *a00 = n00; *a01 = n01; *a10 = n10; *a11 = n11;
+        }
+        // U <- U J: pair L = tid & 31, rows (tid >> 5) + 8m
+        const int L = tid & 31;
+        const float cL = S.rot_c[L], sL = S.rot_s[L];
+        const int pL = S.rot_p[L], qL = S.rot_q[L];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const int i = (tid >> 5) + 8 * m;
+          const float up = S.U[i * kAS + pL], uq = S.U[i * kAS + qL];
+          S.U[i * kAS + pL] = up * cL - uq * sL;
+          S.U[i * kAS + qL] = up * sL + uq * cL;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // ---- 4. top-r eigenpairs (warp 0), tau ------------------------------------
+  const int r = prm.rank;
+  if (warp == 0) {
+    float v0 = S.A[lane * kAS + lane], v1 = S.A[(lane + 32) * kAS + lane + 32];
+    bool t0 = false, t1 = false;
+    float lam1 = 0.f;
+    for (int k = 0; k < r; ++k) {
+      // candidate of this lane: larger value, ties -> lower index
+      float bv = -INFINITY;
+      int bi = 1 << 30;
+      if (!t0) { bv = v0; bi = lane; }
+      if (!t1 && (v1 > bv)) { bv = v1; bi = lane + 32; }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, o);
+        const int oi = __shfl_xor_sync(kFull, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (bi == lane) t0 = true;
+      if (bi == lane + 32) t1 = true;
+      if (k == 0) lam1 = bv;
+      if (lane == 0) {
+        const bool keep = bv > 0.f && bv > kDropRel * lam1;
+        S.lam[k] = keep ? bv : 0.f;
+        S.order[k] = bi;
+      }
+    }
+    float rest = (t0 ? 0.f : fmaxf(v0, 0.f)) + (t1 ? 0.f : fmaxf(v1, 0.f));
+    rest = group_sum<32>(rest);
+    if (lane == 0) S.tau = rest;
+  }
+  __syncthreads();
+
+  // ---- 5. record: W[0] = mu, W[1+k] = v_k, C[c][i][e] = u_ik sigma_k ----------
+  T* rec = reinterpret_cast<T*>(static_cast<unsigned char*>(prm.summaries) +
+                                (size_t(blk) * prm.n_kv_heads + h) * prm.rec_bytes);
+  if (tid < kHeadDim) {
+    const int t = tid;
+    st_elem(rec + t, S.mu[t]);
+    float v[RP];
+#pragma unroll
+    for (int k = 0; k < RP; ++k) v[k] = 0.f;
+    for (int i = 0; i < kPageSize; ++i) {
+      const float dit = S.D[i * kDS + t];
+#pragma unroll
+      for (int k = 0; k < RP; ++k)
+        if (k < r) v[k] += dit * S.U[i * kAS + S.order[k]];
+    }
+#pragma unroll
+    for (int k = 0; k < RP; ++k) {
+      const float lam = k < r ? S.lam[k] : 0.f;
+      st_elem(rec + (1 + k) * kHeadDim + t, lam > 0.f ? v[k] * rsqrtf(lam) : 0.f);
+    }
+  } else {
+    T* C = rec + rec_w_elems(RP);
+    for (int idx = tid - kHeadDim; idx < kPageSize * RP; idx += kBuildThreads - kHeadDim) {
+      const int i = idx / RP, k = idx % RP;
+      const float lam = k < r ? S.lam[k] : 0.f;
+      const float c = lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
+      st_elem(C + ((k >> 2) * kPageSize + i) * 4 + (k & 3), c);
+    }
+  }
+  if (tid == 0) {
+    if (prm.tail_energy) prm.tail_energy[out_idx] = S.tau;
+    if (prm.status) prm.status[out_idx] = sweeps | (converged ? 0 : (LOCKS_DEV_NOT_CONVERGED << 16));
+  }
+}
+
+template <int RP, typename T>
+int launch_t(const BuildParams& p, cudaStream_t stream) {
+  const size_t smem = sizeof(BuildSmem);
+  auto kern = build_kernel<RP, T>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+      cudaSuccess)
+    return LOCKS_ERR_CUDA;
+  kern<<<dim3(p.n_blocks, p.n_kv_heads), kBuildThreads, smem, stream>>>(p);
+  return cudaPeekAtLastError() == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_build(const BuildParams& p, int RP, int dtype, cudaStream_t stream) {
+  const bool f32 = dtype == LOCKS_SUMMARY_F32;
+  switch (RP) {
+    case 4: return f32 ? launch_t<4, float>(p, stream) : launch_t<4, __nv_bfloat16>(p, stream);
+    case 8: return f32 ? launch_t<8, float>(p, stream) : launch_t<8, __nv_bfloat16>(p, stream);
+    case 16: return f32 ? launch_t<16, float>(p, stream) : launch_t<16, __nv_bfloat16>(p, stream);
+    default: return LOCKS_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace locks

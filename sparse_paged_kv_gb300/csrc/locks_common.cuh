@@ -1,0 +1,192 @@
+// Device helpers shared by the Locks kernels (sm_103a).
+//
+// * 1-D bulk copies global -> shared (cp.async.bulk) completing on an mbarrier
+//   with a transaction count;
+// * bounded mbarrier waits: every wait gives up after a wall-clock limit,
+//   records LOCKS_DEV_WAIT_TIMEOUT and lets the caller skip the work;
+// * warp "transpose" reductions: N per-lane partial sums are reduced across
+//   the lanes of a warp (or of an aligned lane group) with N-1 shuffles in
+//   total, each lane ending with the full sums of its share of the N values.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/locks.h"
+
+namespace locks {
+
+constexpr int kHeadDim = 128;
+constexpr int kPageSize = 64;
+constexpr unsigned kFull = 0xffffffffu;
+// A bounded wait on a copy gives up after this many nanoseconds.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__host__ __device__ constexpr int rank_cap(int r) { return r <= 4 ? 4 : (r <= 8 ? 8 : 16); }
+
+// Record geometry (element counts); see the record description in locks.h.
+__host__ __device__ constexpr int rec_w_elems(int rp) { return (rp + 1) * kHeadDim; }
+__host__ __device__ constexpr int rec_elems(int rp, int B) { return (rp + 1) * kHeadDim + rp * B; }
+
+// ---------------------------------------------------------------------------
+// status words
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void flag_status(int32_t* status, int32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk copy
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar` to complete; false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global to
+// shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// bf16 helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float4 bf16x4_to_f4(uint2 w) {
+  return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+}
+
+__device__ __forceinline__ float ld_elem(const float* p) { return *p; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// four consecutive elements (16 B of float / 8 B of bf16) from shared memory
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  return bf16x4_to_f4(*reinterpret_cast<const uint2*>(p));
+}
+
+__device__ __forceinline__ void st_elem(float* p, float v) { *p = v; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------
+// packed fp32 FMA (two lanes of fp32 per instruction on sm_100+)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long ra, rb, rc, rd;
+  ra = *reinterpret_cast<unsigned long long*>(&a);
+  rb = *reinterpret_cast<unsigned long long*>(&b);
+  rc = *reinterpret_cast<unsigned long long*>(&c);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  return *reinterpret_cast<float2*>(&rd);
+}
+
+// ---------------------------------------------------------------------------
+// Transposed warp reduction.
+//
+// Every lane of an aligned group of WIDTH lanes (a power of two <= 32) holds
+// N partial sums v[0..N) (N a power of two).  After the call, with
+// S = min(N, WIDTH), lane l of the group holds in v[0 .. N/S) the group-wide
+// sums of the values with indices  (l % WIDTH) / (WIDTH / S) * (N / S) + e.
+// It costs N/2 + N/4 + ... shuffles while N halves, then one butterfly
+// shuffle per remaining lane bit.
+// ---------------------------------------------------------------------------
+template <int N, int OFF>
+struct TransposeReduce {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (OFF >= 1) {
+      if constexpr (N > 1) {
+        constexpr int H = N / 2;
+        const bool upper = (lane & OFF) != 0;
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float send = upper ? v[i] : v[i + H];
+          const float keep = upper ? v[i + H] : v[i];
+          v[i] = keep + __shfl_xor_sync(kFull, send, OFF);
+        }
+        TransposeReduce<H, OFF / 2>::run(v, lane);
+      } else {
+        v[0] += __shfl_xor_sync(kFull, v[0], OFF);
+        TransposeReduce<1, OFF / 2>::run(v, lane);
+      }
+    }
+  }
+};
+
+// Plain butterfly max / sum over an aligned group of WIDTH lanes.
+template <int WIDTH>
+__device__ __forceinline__ float group_max(float x) {
+#pragma unroll
+  for (int o = WIDTH / 2; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
+  return x;
+}
+template <int WIDTH>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+  for (int o = WIDTH / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+
+// Online log-sum-exp state merge: (m, s) represents s * exp(m) (natural log).
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  s = s * __expf(m - M) + s2 * __expf(m2 - M);
+  m = M;
+}
+
+}  // namespace locks

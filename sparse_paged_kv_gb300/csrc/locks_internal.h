@@ -1,0 +1,69 @@
+// Parameter blocks and launchers shared between the C-ABI entry points
+// (locks_api.cu) and the kernels.  Internal to the library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace locks {
+
+constexpr size_t kMaxDynSmem = 227 * 1024;
+// floats per (split, head) decode partial: m, l, two pad words, acc[head_dim]
+constexpr int kPartStride = 4 + 128;
+
+struct SelectParams {
+  const __nv_bfloat16* q;        // [batch][H_q][d]
+  const void* summaries;         // record pool
+  const int32_t* block_table;    // [batch][max_pages]
+  const int32_t* seq_lens;       // [batch]
+  int32_t* selected;             // [batch][H_kv][k]
+  float* page_lse;               // nullable [batch][H_q][max_pages]
+  float* page_share;             // nullable [batch][H_kv][max_pages]
+  int32_t* status;               // nullable
+  float* ws_scores;              // [U][max_pages][G]
+  float2* ws_part;               // [U][n_chunks_max][G]
+  int32_t* ws_ticket;            // [U]
+  size_t rec_bytes;
+  int n_kv_heads, max_pages, num_blocks;
+  int k;                         // page budget
+  int chunk_pages, n_chunks_max;
+  float scale, scale_log2;
+};
+
+struct DecodeParams {
+  const __nv_bfloat16* q;        // [batch][H_q][d]
+  const __nv_bfloat16* k_cache;  // [num_blocks][H_kv][B][d]
+  const __nv_bfloat16* v_cache;
+  const int32_t* block_table;    // [batch][max_pages]
+  const int32_t* seq_lens;       // [batch]
+  const int32_t* selected;       // nullable: [batch][H_kv][k]; NULL = every page
+  __nv_bfloat16* out;            // [batch][H_q][d]
+  float* out_lse;                // nullable [batch][H_q]
+  int32_t* status;               // nullable
+  float* ws_part;                // [U][n_splits_max][G][kPartStride]
+  int32_t* ws_ticket;            // [U]
+  int n_kv_heads, max_pages, num_blocks;
+  int k;                         // row stride of `selected`
+  int pages_per_split, n_splits_max;
+  float scale, scale_log2;
+};
+
+struct BuildParams {
+  const __nv_bfloat16* k_cache;  // [num_blocks][H_kv][B][d]
+  const int32_t* block_ids;      // [n_blocks]
+  void* summaries;
+  float* tail_energy;            // nullable [n_blocks][H_kv]
+  int32_t* status;               // nullable [n_blocks][H_kv]
+  size_t rec_bytes;
+  int n_blocks, n_kv_heads, num_blocks, rank, max_sweeps;
+};
+
+int select_chunk_pages(int max_pages);
+int launch_select(const SelectParams& p, int G, int RP, int dtype, int grid_x, int grid_y,
+                  cudaStream_t stream);
+int launch_decode(const DecodeParams& p, int G, int grid_x, int grid_y, cudaStream_t stream);
+int launch_build(const BuildParams& p, int RP, int dtype, cudaStream_t stream);
+
+}  // namespace locks

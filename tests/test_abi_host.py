@@ -1,0 +1,136 @@
+"""The C-ABI library on the host: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments before launching anything (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_paged_kv_gb300 import binding as B
+from sparse_paged_kv_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "locks.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build_lib.build()
+    return B.load_library(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(locks_[a-z_0-9]+)\s*\(", src)))
+
+
+def cfg(**kw):
+    base = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=64, rank=8,
+                max_pages=64, num_blocks=200, summary_dtype=B.LOCKS_SUMMARY_F32)
+    base.update(kw)
+    return B.LocksConfig(**base)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.locks_abi_version() == 1
+
+
+def test_struct_layout_matches_header(lib):
+    assert ctypes.sizeof(B.locks_cfg_t) == 9 * 4
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct locks_cfg \{(.*?)\} locks_cfg_t;", src, re.S).group(1)
+    fields = re.findall(r"int32_t\s+(\w+);", body)
+    assert fields == [f[0] for f in B.locks_cfg_t._fields_]
+
+
+def test_record_bytes(lib):
+    assert B.summary_record_bytes(cfg()) == ((8 + 1) * 128 + 8 * 64) * 4 == 6656
+    assert B.summary_record_bytes(cfg(summary_dtype=B.LOCKS_SUMMARY_BF16)) == 3328
+    assert B.summary_record_bytes(cfg(rank=3)) == ((4 + 1) * 128 + 4 * 64) * 4
+    assert B.summary_record_bytes(cfg(rank=15)) == ((16 + 1) * 128 + 16 * 64) * 4
+    assert B.summary_record_bytes(cfg(head_dim=64)) == 0          # unsupported
+    assert B.summary_record_bytes(cfg(n_q_heads=6, n_kv_heads=2)) == 0   # G = 3
+
+
+def test_workspace_sizes_grow_with_shape(lib):
+    a = B.select_workspace_bytes(cfg(), 512)
+    b = B.select_workspace_bytes(cfg(batch=4), 512)
+    assert 0 < a < b
+    s = B.decode_workspace_bytes(cfg(), 8)
+    d = B.decode_workspace_bytes(cfg(), 64)
+    assert 0 < s <= d
+    assert B.decode_workspace_bytes(cfg(), -1) == 0
+
+
+FAKE = 0x10000   # never dereferenced: every call below returns before a launch
+
+
+def _select(lib, c, budget=512, ws_bytes=1 << 30, **over):
+    args = dict(q=FAKE, summ=FAKE, bt=FAKE, sl=FAKE, sel=FAKE, ws=FAKE)
+    args.update(over)
+    return lib.locks_select(ctypes.byref(c.c()), args["q"], args["summ"], args["bt"], args["sl"],
+                            budget, args["sel"], None, None, args["ws"], ws_bytes, None, None)
+
+
+def test_select_validation(lib):
+    assert _select(lib, cfg(), budget=64) == B.LOCKS_ERR_INVALID_ARG        # k = 1
+    assert _select(lib, cfg(), budget=0) == B.LOCKS_ERR_INVALID_ARG
+    assert _select(lib, cfg(), ws_bytes=16) == B.LOCKS_ERR_WORKSPACE
+    assert _select(lib, cfg(), q=None) == B.LOCKS_ERR_INVALID_ARG
+    assert _select(lib, cfg(head_dim=96)) == B.LOCKS_ERR_UNSUPPORTED
+    assert _select(lib, cfg(page_size=16)) == B.LOCKS_ERR_UNSUPPORTED
+    assert _select(lib, cfg(rank=17)) == B.LOCKS_ERR_UNSUPPORTED
+    assert _select(lib, cfg(n_q_heads=7)) == B.LOCKS_ERR_INVALID_ARG
+    assert _select(lib, cfg(summary_dtype=5)) == B.LOCKS_ERR_INVALID_ARG
+    assert _select(lib, cfg(), budget=64 * 300) == B.LOCKS_ERR_UNSUPPORTED   # k > 256
+    assert _select(lib, cfg(batch=0)) == B.LOCKS_OK                       # nothing to do
+    assert lib.locks_select(None, FAKE, FAKE, FAKE, FAKE, 512, FAKE, None, None, FAKE, 1 << 30,
+                            None, None) == B.LOCKS_ERR_INVALID_ARG
+
+
+def test_decode_and_build_validation(lib):
+    c = cfg()
+    ws = B.decode_workspace_bytes(c, 8)
+    assert lib.locks_sparse_decode(ctypes.byref(c.c()), FAKE, FAKE, FAKE, FAKE, FAKE, None, 8,
+                                   FAKE, None, FAKE, ws, None, None) == B.LOCKS_ERR_INVALID_ARG
+    assert lib.locks_sparse_decode(ctypes.byref(c.c()), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8,
+                                   FAKE, None, FAKE, ws - 1, None, None) == B.LOCKS_ERR_WORKSPACE
+    assert lib.locks_dense_decode(ctypes.byref(c.c()), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                  FAKE, 16, None, None) == B.LOCKS_ERR_WORKSPACE
+    assert lib.locks_dense_decode(ctypes.byref(cfg(batch=0).c()), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, None, FAKE, 0, None, None) == B.LOCKS_OK
+    assert lib.locks_build_summaries(ctypes.byref(c.c()), FAKE, FAKE, -1, FAKE, None, None, 0,
+                                     None) == B.LOCKS_ERR_INVALID_ARG
+    assert lib.locks_build_summaries(ctypes.byref(c.c()), FAKE, FAKE, 0, FAKE, None, None, 0,
+                                     None) == B.LOCKS_OK
+    assert lib.locks_build_summaries(ctypes.byref(c.c()), None, FAKE, 4, FAKE, None, None, 0,
+                                     None) == B.LOCKS_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, 99):
+        assert isinstance(lib.locks_status_string(code), bytes)
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(B.LocksLibraryMissing):
+        B.load_library(str(tmp_path / "missing.so"))
+
+
+def test_unpack_records_layout():
+    import numpy as np
+    c = cfg(rank=8)
+    R, d, Bp = 8, 128, 64
+    mu = np.arange(d, dtype=np.float32)
+    V = np.random.default_rng(0).standard_normal((d, R)).astype(np.float32)
+    C = np.random.default_rng(1).standard_normal((Bp, R)).astype(np.float32)
+    W = np.concatenate([mu[None], V.T], axis=0).reshape(-1)
+    C4 = C.reshape(Bp, R // 4, 4).transpose(1, 0, 2).reshape(-1)
+    raw = np.concatenate([W, C4]).view(np.uint8)
+    m2, V2, C2 = B.unpack_records(raw[None], c)
+    assert np.array_equal(m2[0], mu) and np.array_equal(V2[0], V) and np.array_equal(C2[0], C)

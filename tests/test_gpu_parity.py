@@ -1,0 +1,111 @@
+"""CUDA path against the fp64 oracle on small seeded workloads (several tiles,
+ragged tails, GQA group sizes 1..8, ranks 4..16, the degenerate cases)."""
+import numpy as np
+import pytest
+
+import workloads as W
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+TINY = W.get("tiny")
+
+CASES = {
+    "tiny": TINY,
+    # partial tail page (n = 65), n <= k, n = k + 1, single page, empty sequence
+    "ragged": TINY.with_(batch=5, seq_lens=(4096 + 37, 200, 64 * 9, 40, 0), seed=2001),
+    "group1": TINY.with_(n_q_heads=2, n_kv_heads=2, seed=2002),
+    "group2": TINY.with_(n_q_heads=4, n_kv_heads=2, seed=2003),
+    "group8": TINY.with_(n_q_heads=16, n_kv_heads=2, seed=2004),
+    "k2_forced_only": TINY.with_(budget_tokens=100, seed=2005),
+    "rank4": TINY.with_(rank=4, seed=2006),
+    "rank3": TINY.with_(rank=3, seed=2007),
+    "rank16": TINY.with_(rank=16, seed=2008),
+    # many selection chunks per unit, global component, 1% carriers
+    "multichunk": TINY.with_(context=64 * 300, global_rank=16, carrier_count=None,
+                             carrier_frac=0.01, budget_tokens=2048, seed=2009),
+    "batch_heads": TINY.with_(batch=3, n_q_heads=16, n_kv_heads=4, context=64 * 70,
+                              global_rank=16, seed=2010),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    from sparse_paged_kv_gb300 import binding, build_lib
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    binding.load_library(build_lib.build())
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_parity(name):
+    inputs = W.generate(CASES[name])
+    rep, layer, snap = P.run_case(inputs)
+    rep.check()
+    assert rep.units == CASES[name].batch * CASES[name].n_kv_heads
+    print(f"{name}: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} dense "
+          f"{rep.max_dense_err:.2e} recon {rep.max_recon_rel:.2e} sigma {rep.max_sigma_rel:.2e} "
+          f"degenerate {rep.degenerate} ties {rep.tie_diffs}")
+
+
+def test_empty_sequence_outputs_zero():
+    inputs = W.generate(CASES["ragged"])
+    rep, layer, snap = P.run_case(inputs, units=[(4, 0), (4, 1)])
+    rep.check()
+    assert np.all(snap["selected"][4] == -1)
+    assert np.all(snap["out"][4] == 0) and np.all(np.isneginf(snap["out_lse"][4]))
+
+
+def test_repeat_calls_reuse_workspace():
+    """Tickets reset themselves: the same workspace gives the same result twice."""
+    import torch
+    inputs = W.generate(CASES["multichunk"])
+    rep, layer, snap = P.run_case(inputs, units=[(0, 0)])
+    rep.check()
+    for _ in range(3):
+        layer.step()
+        layer.dense_decode()
+    torch.cuda.synchronize()
+    assert np.array_equal(layer.selected.cpu().numpy(), snap["selected"])
+    assert np.array_equal(layer.out.float().cpu().numpy(), snap["out"].astype(np.float32))
+    assert np.array_equal(layer.out_dense.float().cpu().numpy(),
+                          snap["out_dense"].astype(np.float32))
+
+
+def test_bad_block_id_is_flagged_and_skipped():
+    import torch
+    from sparse_paged_kv_gb300 import binding as B
+    inputs = W.generate(TINY.with_(seed=2011))
+    rep, layer, snap = P.run_case(inputs, units=[(0, 0)], dense=False)
+    rep.check()
+    bt = layer.block_table.clone()
+    bt[0, 5] = layer.cfg.num_blocks + 7          # outside the pool
+    layer.block_table = bt
+    layer.status.zero_()
+    layer.step()
+    layer.dense_decode()
+    torch.cuda.synchronize()
+    st = int(layer.status.cpu()[0])
+    assert st & B.LOCKS_DEV_BAD_BLOCK_ID
+    assert not st & B.LOCKS_DEV_WAIT_TIMEOUT
+    assert np.all(np.isfinite(layer.out.float().cpu().numpy()))
+
+
+def test_jacobi_sweep_cap_is_flagged():
+    import torch
+    from sparse_paged_kv_gb300 import binding as B
+    inputs = W.generate(TINY.with_(seed=2012))
+    from sparse_paged_kv_gb300 import runtime
+    layer = runtime.LocksLayer.from_inputs(inputs)
+    ids = runtime.complete_page_blocks(inputs.block_table, inputs.seq_lens, 64)[:8]
+    st = torch.zeros((8, 2), dtype=torch.int32, device="cuda")
+    layer.build(torch.from_numpy(ids).cuda(), status=st, max_sweeps=1)
+    torch.cuda.synchronize()
+    s = st.cpu().numpy()
+    assert np.all((s >> 16) & B.LOCKS_DEV_NOT_CONVERGED)
+    assert np.all((s & 0xFFFF) == 1)
+    layer.build(torch.from_numpy(ids).cuda(), status=st)
+    torch.cuda.synchronize()
+    s = st.cpu().numpy()
+    assert np.all((s >> 16) == 0) and np.all((s & 0xFFFF) <= 20)
