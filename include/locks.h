@@ -190,6 +190,34 @@ int locks_dense_decode(const locks_cfg_t* cfg, const void* q, const void* k_cach
                        void* out, float* out_lse, void* workspace, size_t workspace_bytes,
                        int32_t* status, void* stream);
 
+/*
+ * locks_select_noalloc -- the page selection of locks_select for callers that
+ * cannot allocate device memory.  The paper has no counterpart: this is a
+ * packaging variant, not a step of the method.
+ *
+ * Callers such as a serving engine whose memory pool already owns all of the
+ * GPU, a plugin whose host forbids cudaMalloc on the decode path (it can
+ * synchronise the device and fragment the pool), or an embedded user without
+ * an allocator get the same selection without passing a workspace: the
+ * scratch lives in one fixed device array of LOCKS_SELECT_NOALLOC_MAX_BYTES
+ * inside the library, which every GPU that loads the library keeps until the
+ * process exits.  The call itself allocates and frees nothing.
+ *
+ * Arguments and outputs are those of locks_select, minus the workspace.
+ * Shapes whose locks_select_workspace_bytes(cfg, budget_tokens) exceeds
+ * LOCKS_SELECT_NOALLOC_MAX_BYTES are rejected with LOCKS_ERR_WORKSPACE (for
+ * example, with G = 4, batch x n_kv_heads x max_pages must stay below about
+ * 250,000 pages).  The first call on a device, with that device current,
+ * looks up the array's device address; make that first call before any stream
+ * capture.  Every call clears the scratch it uses on `stream` before selecting.
+ * All calls share the one array: calls that can overlap on the GPU race.
+ */
+#define LOCKS_SELECT_NOALLOC_MAX_BYTES (4u << 20)
+int locks_select_noalloc(const locks_cfg_t* cfg, const void* q, const void* summaries,
+                         const int32_t* block_table, const int32_t* seq_lens,
+                         int32_t budget_tokens, int32_t* selected, float* page_lse,
+                         float* page_share, int32_t* status, void* stream);
+
 /* Static string for a LOCKS_* return code. */
 const char* locks_status_string(int code);
 

@@ -101,6 +101,8 @@ _SIGS = {
                                            ctypes.c_int32, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "locks_dense_decode": (ctypes.c_int, [ctypes.POINTER(locks_cfg_t), _P, _P, _P, _P, _P, _P, _P,
                                           _P, ctypes.c_size_t, _P, _P]),
+    "locks_select_noalloc": (ctypes.c_int, [ctypes.POINTER(locks_cfg_t), _P, _P, _P, _P,
+                                            ctypes.c_int32, _P, _P, _P, _P, _P]),
     "locks_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "locks_abi_version": (ctypes.c_int, []),
 }
@@ -190,6 +192,18 @@ def locks_select(cfg: LocksConfig, q, summaries, block_table, seq_lens, budget_t
         int(budget_tokens), _ptr(selected), _ptr(page_lse), _ptr(page_share), _ptr(workspace),
         int(wsb), _ptr(status), _stream(stream))
     _check("locks_select", rc)
+
+
+def locks_select_noalloc(cfg: LocksConfig, q, summaries, block_table, seq_lens,
+                         budget_tokens: int, selected, page_lse=None, page_share=None,
+                         status=None, stream=None) -> None:
+    """locks_select without a workspace: the scratch is a fixed device array
+    inside the library (for callers that cannot allocate device memory)."""
+    rc = load_library().locks_select_noalloc(
+        ctypes.byref(cfg.c()), _ptr(q), _ptr(summaries), _ptr(block_table), _ptr(seq_lens),
+        int(budget_tokens), _ptr(selected), _ptr(page_lse), _ptr(page_share), _ptr(status),
+        _stream(stream))
+    _check("locks_select_noalloc", rc)
 
 
 def locks_sparse_decode(cfg: LocksConfig, q, k_cache, v_cache, block_table, seq_lens, selected,
