@@ -39,26 +39,6 @@ int page_budget(int budget_tokens, int page_size) {
   return (budget_tokens + page_size - 1) / page_size;   // k = ceil(b / B)
 }
 
-// ---- select workspace -------------------------------------------------------
-struct SelectLayout {
-  size_t scores, part, ticket, total;
-  int chunk_pages, n_chunks_max;
-};
-
-SelectLayout select_layout(const locks_cfg_t* c) {
-  SelectLayout L;
-  const int G = group_of(c);
-  const size_t U = size_t(c->batch) * c->n_kv_heads;
-  L.chunk_pages = locks::select_chunk_pages(c->max_pages);
-  const int max_cand = c->max_pages > 2 ? c->max_pages - 2 : 0;
-  L.n_chunks_max = max_cand > 0 ? (max_cand + L.chunk_pages - 1) / L.chunk_pages : 1;
-  L.scores = 0;
-  L.part = L.scores + align_up(U * c->max_pages * G * sizeof(float));
-  L.ticket = L.part + align_up(U * L.n_chunks_max * G * sizeof(float2));
-  L.total = L.ticket + align_up(U * sizeof(int32_t));
-  return L;
-}
-
 // ---- decode workspace -------------------------------------------------------
 struct DecodeLayout {
   size_t part, ticket, total;
@@ -130,9 +110,12 @@ size_t locks_summary_record_bytes(const locks_cfg_t* cfg) {
 }
 
 size_t locks_select_workspace_bytes(const locks_cfg_t* cfg, int32_t budget_tokens) {
-  (void)budget_tokens;
   if (check_cfg(cfg) != LOCKS_OK) return 0;
-  return select_layout(cfg).total;
+  const int k = page_budget(budget_tokens, cfg->page_size);
+  if (budget_tokens <= 0 || k < 2) return 0;
+  if (cfg->batch == 0) return 0;
+  return locks::select_geometry(cfg->batch * cfg->n_kv_heads, cfg->max_pages, group_of(cfg), k)
+      .total;
 }
 
 size_t locks_decode_workspace_bytes(const locks_cfg_t* cfg, int32_t n_pages) {
@@ -176,7 +159,8 @@ int locks_select(const locks_cfg_t* cfg, const void* q, const void* summaries,
   if (cfg->batch == 0) return LOCKS_OK;
   if (!q || !summaries || !block_table || !seq_lens || !selected || !workspace)
     return LOCKS_ERR_INVALID_ARG;
-  const SelectLayout L = select_layout(cfg);
+  const int U = cfg->batch * cfg->n_kv_heads;
+  const locks::SelectGeom L = locks::select_geometry(U, cfg->max_pages, group_of(cfg), k);
   if (workspace_bytes < L.total) return LOCKS_ERR_WORKSPACE;
   locks::SelectParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -188,21 +172,26 @@ int locks_select(const locks_cfg_t* cfg, const void* q, const void* summaries,
   p.page_share = page_share;
   p.status = status;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  p.ws_scores = reinterpret_cast<float*>(ws + L.scores);
-  p.ws_part = reinterpret_cast<float2*>(ws + L.part);
-  p.ws_ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
+  p.ws_scores = reinterpret_cast<float*>(ws + L.off_scores);
+  p.ws_part = reinterpret_cast<float2*>(ws + L.off_part);
+  p.ws_cand = reinterpret_cast<uint2*>(ws + L.off_cand);
+  p.ws_ticket = reinterpret_cast<int32_t*>(ws + L.off_ticket);
   p.rec_bytes = locks_summary_record_bytes(cfg);
+  p.units = U;
   p.n_kv_heads = cfg->n_kv_heads;
   p.max_pages = cfg->max_pages;
   p.num_blocks = cfg->num_blocks;
   p.k = k;
-  p.chunk_pages = L.chunk_pages;
-  p.n_chunks_max = L.n_chunks_max;
+  p.mc = L.mc;
+  p.per_cta = L.per_cta;
+  p.nseg_max = L.nseg_max;
+  p.slice = L.slice;
+  p.nslices_max = L.nslices_max;
+  p.fin_cap = L.fin_cap;
   p.scale = float(1.0 / std::sqrt(double(cfg->head_dim)));
   p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(cfg->head_dim)));
-  const int U = cfg->batch * cfg->n_kv_heads;
   return locks::launch_select(p, group_of(cfg), locks::rank_cap(cfg->rank), cfg->summary_dtype,
-                              L.n_chunks_max, U, static_cast<cudaStream_t>(stream));
+                              L.n_score_ctas, L.nslices_max, static_cast<cudaStream_t>(stream));
 }
 
 int locks_sparse_decode(const locks_cfg_t* cfg, const void* q, const void* k_cache,

@@ -124,6 +124,21 @@ __device__ __forceinline__ void st_elem(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // ---------------------------------------------------------------------------
+// fast base-2 exponent / logarithm (the PTX approximate instructions)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
 // packed fp32 FMA (two lanes of fp32 per instruction on sm_100+)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -132,6 +147,14 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   rb = *reinterpret_cast<unsigned long long*>(&b);
   rc = *reinterpret_cast<unsigned long long*>(&c);
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  return *reinterpret_cast<float2*>(&rd);
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  unsigned long long ra, rb, rd;
+  ra = *reinterpret_cast<unsigned long long*>(&a);
+  rb = *reinterpret_cast<unsigned long long*>(&b);
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
   return *reinterpret_cast<float2*>(&rd);
 }
 
@@ -162,6 +185,29 @@ struct TransposeReduce {
       } else {
         v[0] += __shfl_xor_sync(kFull, v[0], OFF);
         TransposeReduce<1, OFF / 2>::run(v, lane);
+      }
+    }
+  }
+};
+
+// Transposed max: as TransposeReduce with max in place of +.
+template <int N, int OFF>
+struct TransposeMax {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (OFF >= 1) {
+      if constexpr (N > 1) {
+        constexpr int H = N / 2;
+        const bool upper = (lane & OFF) != 0;
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float send = upper ? v[i] : v[i + H];
+          const float keep = upper ? v[i + H] : v[i];
+          v[i] = fmaxf(keep, __shfl_xor_sync(kFull, send, OFF));
+        }
+        TransposeMax<H, OFF / 2>::run(v, lane);
+      } else {
+        v[0] = fmaxf(v[0], __shfl_xor_sync(kFull, v[0], OFF));
+        TransposeMax<1, OFF / 2>::run(v, lane);
       }
     }
   }

@@ -31,6 +31,14 @@ constexpr int kRowBytes = kHeadDim * 2;                    // 256
 constexpr int kPageBytes = kPageSize * kRowBytes;          // 16 KiB
 constexpr int kSlotBytes = 2 * kPageBytes;                 // K then V
 
+constexpr int kMaxPagesPerSplit = 64;
+
+// float max through the integer atomics (ordering of IEEE bit patterns)
+__device__ __forceinline__ void atomicMax_float(float* addr, float v) {
+  if (v >= 0.f) atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
+  else atomicMin(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
+}
+
 template <int G>
 __host__ __device__ constexpr int warp_buf_floats() {
   return ((2 * G * kTokPerWarp + 3 * G) + 3) / 4 * 4;
@@ -43,6 +51,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
   const int u = blockIdx.y, sp = blockIdx.x;
   const int b = u / p.n_kv_heads, h = u % p.n_kv_heads;
   constexpr int B = kPageSize;
+
+  // launched as a programmatic dependent of the previous kernel on the stream:
+  // wait for it to finish before reading anything it may have written
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   int seq_len = p.seq_lens[b];
   if (seq_len > p.max_pages * B) {
@@ -65,6 +77,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
   float* wbuf_all = reinterpret_cast<float*>(slot_nv + ((STAGES + 3) / 4) * 4);
   __shared__ int s_is_last;
 
+  __shared__ int s_blk[kMaxPagesPerSplit], s_nv[kMaxPagesPerSplit];
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full + s, 1);
@@ -72,9 +85,23 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
     }
     mbar_fence_init();
   }
+  // page ids of this split: block and valid tokens, checked once
+  const int32_t* bt = p.block_table + size_t(b) * p.max_pages;
+  for (int t = tid; t < cnt; t += kDecThreads) {
+    const int j = p.selected ? p.selected[size_t(u) * p.k + i_lo + t] : i_lo + t;
+    int nv = 0, blk = -1;
+    if (j >= 0 && j < n) {
+      blk = bt[j];
+      if (blk >= 0 && blk < p.num_blocks) nv = min(B, seq_len - j * B);
+      else flag_status(p.status, LOCKS_DEV_BAD_BLOCK_ID);
+    } else if (j >= n) {
+      flag_status(p.status, LOCKS_DEV_BAD_PAGE_ID);
+    }
+    s_blk[t] = blk;
+    s_nv[t] = nv;
+  }
   __syncthreads();
 
-  const int32_t* bt = p.block_table + size_t(b) * p.max_pages;
   float acc[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
@@ -88,22 +115,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      const int32_t* sel = p.selected ? p.selected + size_t(u) * p.k : nullptr;
       for (int i = 0; i < cnt; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES && !mbar_wait_bounded(empty + s, ((i / STAGES) - 1) & 1)) {
           flag_status(p.status, LOCKS_DEV_WAIT_TIMEOUT);
           break;
         }
-        const int j = sel ? sel[i_lo + i] : i_lo + i;
-        int nv = 0, blk = -1;
-        if (j >= 0 && j < n) {
-          blk = bt[j];
-          if (blk >= 0 && blk < p.num_blocks) nv = min(B, seq_len - j * B);
-          else flag_status(p.status, LOCKS_DEV_BAD_BLOCK_ID);
-        } else if (j >= n) {
-          flag_status(p.status, LOCKS_DEV_BAD_PAGE_ID);
-        }
+        const int nv = s_nv[i], blk = s_blk[i];
         slot_nv[s] = nv;
         if (nv > 0) {
           const size_t off = (size_t(blk) * p.n_kv_heads + h) * (B * kHeadDim);
@@ -282,22 +300,32 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
   __threadfence();
 
   // ---- last split of the unit: merge every split -----------------------------
+  // per-head maximum over the splits first (all loads in parallel) ...
+  __shared__ float s_mmax[8];
+  if (tid < G) s_mmax[tid] = -INFINITY;
+  __syncthreads();
+  for (int t = tid; t < nsplits * G; t += kDecThreads) {
+    const int s2 = t / G, g = t % G;
+    const float m2 = __ldcg(p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + g) * part_stride);
+    if (m2 != -INFINITY) atomicMax_float(s_mmax + g, m2);
+  }
+  __syncthreads();
+  // ... then the rescaled sums, whose loads no longer depend on each other
   for (int t = tid; t < G * 32; t += kDecThreads) {
     const int g = t >> 5, l4 = t & 31;
-    float M = -INFINITY, L = 0.f;
+    const float M = s_mmax[g];
+    float L = 0.f;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s2 = 0; s2 < nsplits; ++s2) {
-      const float* pg = p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + g) * part_stride;
-      const float m2 = __ldcg(pg);
-      if (m2 == -INFINITY) continue;
-      const float l2 = __ldcg(pg + 1);
-      const float4 a2 = __ldcg(reinterpret_cast<const float4*>(pg + 4 + 4 * l4));
-      const float Mn = fmaxf(M, m2);
-      const float f1 = exp2f((M - Mn) * p.scale_log2), f2 = exp2f((m2 - Mn) * p.scale_log2);
-      L = L * f1 + l2 * f2;
-      A.x = A.x * f1 + a2.x * f2; A.y = A.y * f1 + a2.y * f2;
-      A.z = A.z * f1 + a2.z * f2; A.w = A.w * f1 + a2.w * f2;
-      M = Mn;
+    if (M != -INFINITY) {
+#pragma unroll 8
+      for (int s2 = 0; s2 < nsplits; ++s2) {
+        const float* pg = p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + g) * part_stride;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg));
+        const float4 a2 = __ldcg(reinterpret_cast<const float4*>(pg + 4 + 4 * l4));
+        const float f = ml.x == -INFINITY ? 0.f : exp2f((ml.x - M) * p.scale_log2);
+        L += ml.y * f;
+        A.x += a2.x * f; A.y += a2.y * f; A.z += a2.z * f; A.w += a2.w * f;
+      }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     __nv_bfloat16* o = p.out + (size_t(b) * (p.n_kv_heads * G) + h * G + g) * kHeadDim + 4 * l4;
@@ -324,8 +352,17 @@ int launch_g(const DecodeParams& p, int gx, int gy, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return LOCKS_ERR_CUDA;
-  kern<<<dim3(gx, gy), kDecThreads, smem, stream>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(gx, gy);
+  lc.blockDim = dim3(kDecThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kern, p) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
 }
 
 }  // namespace

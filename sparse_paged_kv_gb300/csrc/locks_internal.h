@@ -23,13 +23,28 @@ struct SelectParams {
   float* page_share;             // nullable [batch][H_kv][max_pages]
   int32_t* status;               // nullable
   float* ws_scores;              // [U][max_pages][G]
-  float2* ws_part;               // [U][n_chunks_max][G]
+  float2* ws_part;               // [U][nseg_max][G] log-sum-exp partials
+  uint2* ws_cand;                // [U][nslices_max][k-2] slice winners (key, page)
   int32_t* ws_ticket;            // [U]
   size_t rec_bytes;
-  int n_kv_heads, max_pages, num_blocks;
+  int units, n_kv_heads, max_pages, num_blocks;
   int k;                         // page budget
-  int chunk_pages, n_chunks_max;
+  int mc, per_cta, nseg_max;     // score kernel geometry (see select_geometry)
+  int slice, nslices_max, fin_cap;
   float scale, scale_log2;
+};
+
+// Geometry of locks_select for a shape; the workspace size and the launch
+// both come from here.
+struct SelectGeom {
+  int mc;            // candidate slots per unit (even)
+  int per_cta;       // slots per score CTA (even)
+  int n_score_ctas;
+  int nseg_max;      // log-sum-exp partial slots per unit
+  int slice;         // candidates per finalize CTA
+  int nslices_max;
+  int fin_cap;       // finalize shared-memory entries
+  size_t off_scores, off_part, off_cand, off_ticket, total;
 };
 
 struct DecodeParams {
@@ -60,9 +75,9 @@ struct BuildParams {
   int n_blocks, n_kv_heads, num_blocks, rank, max_sweeps;
 };
 
-int select_chunk_pages(int max_pages);
-int launch_select(const SelectParams& p, int G, int RP, int dtype, int grid_x, int grid_y,
-                  cudaStream_t stream);
+SelectGeom select_geometry(int units, int max_pages, int G, int k);
+int launch_select(const SelectParams& p, int G, int RP, int dtype, int n_score_ctas,
+                  int n_slices, cudaStream_t stream);
 int launch_decode(const DecodeParams& p, int G, int grid_x, int grid_y, cudaStream_t stream);
 int launch_build(const BuildParams& p, int RP, int dtype, cudaStream_t stream);
 

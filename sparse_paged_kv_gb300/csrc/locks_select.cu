@@ -3,24 +3,32 @@
 // "Locks: Page-Local Compact Key Summaries for Efficient Long-Context
 // Decoding", section 4 ("Score") and Cor. 3.
 //
-// One grid covers every (sequence b, KV head h) "unit".  CTA (c, u) scores
-// the c-th chunk of unit u's candidate pages.  Each warp owns a ring of
-// STAGES shared-memory slots; lane 0 streams the page summary records of the
-// warp's pages into them with 1-D bulk copies, and the whole warp scores one
-// page per step:
+// Two kernels, the second launched as a programmatic dependent of the first:
 //
-//   lane l holds dims [4l, 4l+4) of the G group queries, dots them with the
-//   centroid and basis rows (a_g = q_g.mu, p_gk = q_g.v_k), the G*R partial
-//   dot products are reduced across the warp with a transposed reduction,
-//   broadcast through shared memory, and lane l then forms the reconstructed
-//   logits of tokens l and l+32 for every head and reduces them by
-//   log-sum-exp.
+// score_kernel (persistent): the candidate pages of every (sequence b, KV
+// head h) "unit" are laid end to end (mc slots per unit) and every CTA takes
+// one contiguous, equal range of slots.  Each of its 4 warps owns a
+// two-stage shared-memory ring of page-pair slots; lane 0 streams the summary
+// records of the warp's next two pages into a slot with 1-D bulk copies, and
+// each half-warp (16 lanes) scores one page of the pair:
+//   lane l of a half holds dims [4l, 4l+4) and [64+4l, 64+4l+4) of the G
+//   group queries and dots them with the centroid and basis rows
+//   (a_g = q_g.mu, p_gk = q_g.v_k; packed fp32 pairs along the dims); the
+//   G(R+1) partial sums are reduced across the 16 lanes with transposed
+//   reductions; the projections go through shared memory to every lane, which
+//   forms the reconstructed logits of tokens l, l+16, l+32, l+48 for every
+//   head and reduces them by log-sum-exp (transposed max and sum).
+// It writes s_hat per (page, head) and, per warp and unit, the running
+// (max, sum) log-sum-exp of its s_hat values.
 //
-// The CTA writes s_hat per (page, head) and its chunk's per-head (max, sum)
-// log-sum-exp partial.  The last CTA of a unit to finish (an atomic ticket,
-// no waiting) merges the partials into log Z_g, forms the averaged shares
-// m_bar_j of every candidate, finds the (k-2)-th largest by a 4-pass 8-bit
-// radix select over the share bit patterns, and writes the ascending page list.
+// finalize_kernel: CTA (slice, unit) merges the unit's partials into
+// log Z_g, forms the averaged shares m_bar_j of its slice of candidates and
+// keeps the slice's top-(k-2) (4-pass 8-bit radix select over the share bit
+// patterns; ties to the smaller page).  The last slice of the unit (atomic
+// ticket, no waiting) merges the slices' winners the same way and writes the
+// forced pages and the winners in ascending page order.
+#include <mutex>
+
 #include "locks_common.cuh"
 #include "locks_internal.h"
 
@@ -28,13 +36,33 @@ namespace locks {
 
 namespace {
 
-constexpr int kSelWarps = 8;
+constexpr int kSelWarps = 4;
 constexpr int kSelThreads = kSelWarps * 32;
+constexpr int kHalf = 16;                    // lanes per page
+constexpr int kUnitSlots = 16;               // units one score CTA may touch
+constexpr int kFinThreads = 256;
+constexpr int kFinWarps = kFinThreads / 32;
 
-// floats of per-warp broadcast buffer: G*R projections + G centroid terms,
-// padded to 16 bytes
+// floats of one half-warp's projection buffer (G*R, padded to 16 bytes)
 template <int G, int RP>
-__host__ __device__ constexpr int pbuf_stride() { return (G * RP + G + 3) / 4 * 4; }
+__host__ __device__ constexpr int pbuf_stride() { return (G * RP + 3) / 4 * 4; }
+
+// G scores of one page from the workspace (16-byte loads where G allows)
+template <int G>
+__device__ __forceinline__ void ld_scores(const float* src, float (&v)[G]) {
+  if constexpr (G % 4 == 0) {
+#pragma unroll
+    for (int g = 0; g < G; g += 4) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(src + g));
+      v[g] = x.x; v[g + 1] = x.y; v[g + 2] = x.z; v[g + 3] = x.w;
+    }
+  } else if constexpr (G == 2) {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+    v[0] = x.x; v[1] = x.y;
+  } else {
+    v[0] = __ldcg(src);
+  }
+}
 
 __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
 #pragma unroll
@@ -45,197 +73,239 @@ __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
   return x;
 }
 
-// Block-wide exclusive scan of one int per thread; returns the exclusive
-// prefix and writes the block total to *total.  `scratch` holds >= 32 ints.
-__device__ int block_excl_scan(int x, int* scratch, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int incl = warp_incl_scan(x, lane);
-  if (lane == 31) scratch[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int v = lane < kSelWarps ? scratch[lane] : 0;
-    const int vi = warp_incl_scan(v, lane);
-    if (lane < kSelWarps) scratch[lane] = vi - v;
-    if (lane == kSelWarps - 1) scratch[kSelWarps] = vi;
-  }
-  __syncthreads();
-  const int res = scratch[warp] + incl - x;
-  *total = scratch[kSelWarps];
-  __syncthreads();
-  return res;
+__device__ __forceinline__ int unit_seq_len(const SelectParams& p, int b) {
+  int t = p.seq_lens[b];
+  if (t > p.max_pages * kPageSize) t = p.max_pages * kPageSize;
+  return t < 0 ? 0 : t;
+}
+// candidates are the complete pages other than page 0 and page n-1
+__device__ __forceinline__ int cand_count(int seq_len) {
+  const int n = (seq_len + kPageSize - 1) / kPageSize;
+  const int hi = min(n - 1, seq_len / kPageSize);
+  return max(0, hi - 1);
 }
 
-// Scores one page summary `rec` for the G queries held in qv (dims [4l,4l+4)).
-// Returns the G scores s_hat (identical in every lane).
+// q . w over this lane's 8 dims: packed fp32 pairs along the dims, then one add
+__device__ __forceinline__ float dot8(const float4& qa, const float4& qb, const float4& wa,
+                                      const float4& wb) {
+  float2 acc = fmul2(make_float2(qa.x, qa.y), make_float2(wa.x, wa.y));
+  acc = ffma2(make_float2(qa.z, qa.w), make_float2(wa.z, wa.w), acc);
+  acc = ffma2(make_float2(qb.x, qb.y), make_float2(wb.x, wb.y), acc);
+  acc = ffma2(make_float2(qb.z, qb.w), make_float2(wb.z, wb.w), acc);
+  return acc.x + acc.y;
+}
+
+// Scores one page summary `rec` in each half-warp (lane hl = lane % 16 of the
+// half).  Returns s_hat of head hl / (16/G) (identical across that head's lanes).
 template <int G, int RP, typename T>
-__device__ __forceinline__ void score_page(const T* __restrict__ rec, const float4 (&qv)[G],
-                                           float* pbuf, int lane, float scale, float scale_log2,
-                                           float (&shat)[G]) {
+__device__ __forceinline__ float score_page16(const T* __restrict__ rec, const float4 (&qa)[G],
+                                              const float4 (&qb)[G], float* pbuf, int hl,
+                                              float scale, float scale_log2) {
   constexpr int NP = G * RP;                   // basis projections p_{g,k}
-  constexpr int SP = NP < 32 ? NP : 32;
+  constexpr int SP = NP < kHalf ? NP : kHalf;
   constexpr int VP = NP / SP;                  // values a lane holds after the reduction
-  constexpr int SA = G < 32 ? G : 32;
+  constexpr int LG = kHalf / G;                // lanes per head after the G-value reductions
+  const int lane = threadIdx.x & 31;
 
   float pv[NP];
   float av[G];
   {
-    const float4 w = ld4(rec + 4 * lane);      // centroid row
+    const float4 wa = ld4(rec + 4 * hl), wb = ld4(rec + 64 + 4 * hl);   // centroid
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      av[g] = qv[g].x * w.x + qv[g].y * w.y + qv[g].z * w.z + qv[g].w * w.w;
+    for (int g = 0; g < G; ++g) av[g] = dot8(qa[g], qb[g], wa, wb);
   }
 #pragma unroll
   for (int k = 0; k < RP; ++k) {
-    const float4 w = ld4(rec + (1 + k) * kHeadDim + 4 * lane);
+    const float4 wa = ld4(rec + (1 + k) * kHeadDim + 4 * hl);
+    const float4 wb = ld4(rec + (1 + k) * kHeadDim + 64 + 4 * hl);
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      pv[g * RP + k] = qv[g].x * w.x + qv[g].y * w.y + qv[g].z * w.z + qv[g].w * w.w;
+    for (int g = 0; g < G; ++g) pv[g * RP + k] = dot8(qa[g], qb[g], wa, wb);
   }
-  TransposeReduce<NP, 16>::run(pv, lane);
-  TransposeReduce<G, 16>::run(av, lane);
-  // lane l now holds p values [(l / (32/SP)) * VP, +VP) and a value l / (32/SA)
-  if ((lane & (32 / SP - 1)) == 0) {
+  TransposeReduce<NP, kHalf / 2>::run(pv, lane);
+  TransposeReduce<G, kHalf / 2>::run(av, lane);
+  // lane hl holds p values [(hl / (16/SP)) * VP, +VP) and a of head hl / LG
+  if ((hl & (kHalf / SP - 1)) == 0) {
 #pragma unroll
-    for (int e = 0; e < VP; ++e) pbuf[(lane / (32 / SP)) * VP + e] = pv[e];
+    for (int e = 0; e < VP; ++e) pbuf[(hl / (kHalf / SP)) * VP + e] = pv[e];
   }
-  if ((lane & (32 / SA - 1)) == 0) pbuf[NP + lane / (32 / SA)] = av[0];
   __syncwarp();
 
-  // reconstructed logits (before the 1/sqrt(d) scale) of tokens lane, lane+32
+  // reconstructed logits (before the 1/sqrt(d) scale) of tokens hl + 16t
+  constexpr int TPL = kPageSize / kHalf;       // 4 tokens per lane
   const T* C = rec + rec_w_elems(RP);
-  float x[G][2];
+  float4 pr[G][RP / 4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) x[g][0] = x[g][1] = 0.f;
+  for (int g = 0; g < G; ++g)
 #pragma unroll
-  for (int cc = 0; cc < RP / 4; ++cc) {
-    const float4 c0 = ld4(C + (cc * kPageSize + lane) * 4);
-    const float4 c1 = ld4(C + (cc * kPageSize + lane + 32) * 4);
+    for (int cc = 0; cc < RP / 4; ++cc)
+      pr[g][cc] = *reinterpret_cast<const float4*>(pbuf + g * RP + cc * 4);
+  float x[G][TPL];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float4 p = *reinterpret_cast<const float4*>(pbuf + g * RP + cc * 4);
-      x[g][0] += p.x * c0.x + p.y * c0.y + p.z * c0.z + p.w * c0.w;
-      x[g][1] += p.x * c1.x + p.y * c1.y + p.z * c1.z + p.w * c1.w;
+  for (int t = 0; t < TPL; ++t) {
+    float2 acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int cc = 0; cc < RP / 4; ++cc) {
+      const float4 c = ld4(C + (cc * kPageSize + hl + kHalf * t) * 4);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        acc[g] = ffma2(make_float2(pr[g][cc].x, pr[g][cc].y), make_float2(c.x, c.y), acc[g]);
+        acc[g] = ffma2(make_float2(pr[g][cc].z, pr[g][cc].w), make_float2(c.z, c.w), acc[g]);
+      }
     }
+#pragma unroll
+    for (int g = 0; g < G; ++g) x[g][t] = acc[g].x + acc[g].y;
   }
+  // log-sum-exp per head: transposed max, broadcast, exponentials, transposed sum
+  float mx[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    const float m = group_max<32>(fmaxf(x[g][0], x[g][1]));
-    const float e = exp2f((x[g][0] - m) * scale_log2) + exp2f((x[g][1] - m) * scale_log2);
-    const float s = group_sum<32>(e);
-    shat[g] = scale * (pbuf[NP + g] + m) + logf(s);
+    mx[g] = fmaxf(fmaxf(x[g][0], x[g][1]), fmaxf(x[g][2], x[g][3]));
   }
-  __syncwarp();   // pbuf is rewritten by the next page
+  TransposeMax<G, kHalf / 2>::run(mx, lane);   // lane holds the max of head hl / LG
+  const float my_max = mx[0];
+  float ev[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float m = __shfl_sync(kFull, my_max, g * LG, kHalf);
+    const float mc = m * scale_log2;
+    float e = 0.f;
+#pragma unroll
+    for (int t = 0; t < TPL; ++t) e += ex2_approx(fmaf(x[g][t], scale_log2, -mc));
+    ev[g] = e;
+  }
+  TransposeReduce<G, kHalf / 2>::run(ev, lane);   // lane holds the sum of head hl / LG
+  __syncwarp();                                   // pbuf is rewritten by the next page
+  return scale * (av[0] + my_max) + kLn2 * lg2_approx(ev[0]);
 }
 
+
 template <int G, int RP, typename T, int STAGES>
-__global__ void __launch_bounds__(kSelThreads)
-    select_kernel(const SelectParams p) {
+__global__ void __launch_bounds__(kSelThreads, (G >= 8 || G * RP >= 64 || sizeof(T) == 4) ? 2 : 4)
+    score_kernel(const SelectParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
-  const int u = blockIdx.y, chunk = blockIdx.x;
-  const int b = u / p.n_kv_heads, h = u % p.n_kv_heads;
-  const int B = kPageSize;
-
-  // ---- the unit's candidate pages ---------------------------------------
-  int seq_len = p.seq_lens[b];
-  if (seq_len > p.max_pages * B) {
-    if (chunk == 0 && tid == 0) flag_status(p.status, LOCKS_DEV_BAD_SEQ_LEN);
-    seq_len = p.max_pages * B;
-  }
-  if (seq_len < 0) seq_len = 0;
-  const int n = (seq_len + B - 1) / B;
-  const int n_complete = seq_len / B;
-  const int cand_hi = min(n - 1, n_complete);          // candidates are pages 1 .. cand_hi-1
-  const int n_cand = max(0, cand_hi - 1);
-  const int nchunks = max(1, (n_cand + p.chunk_pages - 1) / p.chunk_pages);
-  if (chunk >= nchunks) return;
-  const int c_lo = chunk * p.chunk_pages;
-  const int c_hi = min(n_cand, c_lo + p.chunk_pages);
+  const int half = lane >> 4, hl = lane & 15;
+  constexpr int LG = kHalf / G;
+  const long total = long(p.units) * p.mc;
+  const long f_lo = long(blockIdx.x) * p.per_cta;
+  const long f_hi = min(total, f_lo + p.per_cta);
+  if (f_lo >= f_hi) return;
+  const int n_f = int(f_hi - f_lo);              // even
+  const int u_lo = int(f_lo / p.mc);
+  const int u_hi = int((f_hi - 1) / p.mc);       // u_hi - u_lo < kUnitSlots
 
   // ---- shared memory ------------------------------------------------------
   const size_t rec_bytes = p.rec_bytes;
   unsigned char* ring = smem;
-  const size_t ring_bytes = size_t(kSelWarps) * STAGES * rec_bytes;
+  const size_t ring_bytes = size_t(kSelWarps) * STAGES * 2 * rec_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_bytes);
   float* pbuf_all = reinterpret_cast<float*>(bars + kSelWarps * STAGES);
-  float* pbuf = pbuf_all + warp * pbuf_stride<G, RP>();
-  float2* wpart = reinterpret_cast<float2*>(pbuf_all + kSelWarps * pbuf_stride<G, RP>());
-  __shared__ float s_logz[16];
-  __shared__ int s_is_last;
+  float* pbuf = pbuf_all + (warp * 2 + half) * pbuf_stride<G, RP>();
+  float2* upart = reinterpret_cast<float2*>(pbuf_all + kSelWarps * 2 * pbuf_stride<G, RP>());
+  int* s_blk = reinterpret_cast<int*>(upart + kSelWarps * kUnitSlots * G);   // [n_f]
 
   uint64_t* mybar = bars + warp * STAGES;
-  unsigned char* myring = ring + size_t(warp) * STAGES * rec_bytes;
+  unsigned char* myring = ring + size_t(warp) * STAGES * 2 * rec_bytes;
   if (lane == 0) {
     for (int s = 0; s < STAGES; ++s) mbar_init(mybar + s, 1);
     mbar_fence_init();
   }
-  __syncwarp();
-
-  // group queries, dims [4*lane, 4*lane+4)
-  float4 qv[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint2 w = *reinterpret_cast<const uint2*>(
-        p.q + (size_t(b) * (p.n_kv_heads * G) + h * G + g) * kHeadDim + 4 * lane);
-    qv[g] = bf16x4_to_f4(w);
+  // block id of every slot: >= 0 valid, -1 invalid (flagged), -2 no such candidate
+  for (int t = tid; t < n_f; t += kSelThreads) {
+    const long f = f_lo + t;
+    const int u = int(f / p.mc), idx = int(f % p.mc);
+    const int b = u / p.n_kv_heads;
+    int v = -2;
+    if (idx < cand_count(unit_seq_len(p, b))) {
+      const int blk = p.block_table[size_t(b) * p.max_pages + 1 + idx];
+      v = (blk >= 0 && blk < p.num_blocks) ? blk : -1;
+      if (v == -1) flag_status(p.status, LOCKS_DEV_BAD_BLOCK_ID);
+    }
+    s_blk[t] = v;
   }
+  for (int t = tid; t < kSelWarps * kUnitSlots * G; t += kSelThreads)
+    upart[t] = make_float2(-INFINITY, 0.f);
+  __syncthreads();
 
-  const int my_count = (c_hi - c_lo - warp + kSelWarps - 1) / kSelWarps;   // may be <= 0
-  const int32_t* bt = p.block_table + size_t(b) * p.max_pages;
+  // warp w scores the slot pairs (2q, 2q+1), q = w, w+4, ...; both slots of a
+  // pair belong to the same unit (mc and the range start are even)
+  const int n_pairs = n_f / 2;
+  const int my_count = (n_pairs - warp + kSelWarps - 1) / kSelWarps;   // may be <= 0
   const unsigned char* sum_base = static_cast<const unsigned char*>(p.summaries);
-
-  auto page_of = [&](int i) { return 1 + c_lo + warp + i * kSelWarps; };
   auto issue = [&](int i) {
     const int s = i % STAGES;
-    const int j = page_of(i);
-    const int blk = bt[j];
-    if (blk >= 0 && blk < p.num_blocks) {
-      mbar_arrive_expect_tx(mybar + s, uint32_t(rec_bytes));
-      bulk_g2s(myring + size_t(s) * rec_bytes,
-               sum_base + (size_t(blk) * p.n_kv_heads + h) * rec_bytes, uint32_t(rec_bytes),
-               mybar + s);
+    const int t0 = 2 * (i * kSelWarps + warp);
+    const int h = int((f_lo + t0) / p.mc) % p.n_kv_heads;
+    const int b0 = s_blk[t0], b1 = s_blk[t0 + 1];
+    const uint32_t bytes = uint32_t(rec_bytes) * ((b0 >= 0) + (b1 >= 0));
+    if (bytes) {
+      mbar_arrive_expect_tx(mybar + s, bytes);
+      if (b0 >= 0)
+        bulk_g2s(myring + size_t(2 * s) * rec_bytes,
+                 sum_base + (size_t(b0) * p.n_kv_heads + h) * rec_bytes, uint32_t(rec_bytes),
+                 mybar + s);
+      if (b1 >= 0)
+        bulk_g2s(myring + size_t(2 * s + 1) * rec_bytes,
+                 sum_base + (size_t(b1) * p.n_kv_heads + h) * rec_bytes, uint32_t(rec_bytes),
+                 mybar + s);
     } else {
-      flag_status(p.status, LOCKS_DEV_BAD_BLOCK_ID);
       mbar_arrive(mybar + s);
     }
   };
   if (lane == 0)
     for (int i = 0; i < min(STAGES, my_count); ++i) issue(i);
 
-  // running log-sum-exp of s_hat over this warp's pages; lane g < G tracks head g
-  float zm = -INFINITY, zs = 0.f;
-  float* ws_s = p.ws_scores + size_t(u) * p.max_pages * G;
+  const int my_head = hl / LG;
+  const bool head_lane = (hl % LG) == 0;
+  int cur_u = -1;
+  float zm = -INFINITY, zs = 0.f;              // running LSE of the current unit (head lanes)
+  float4 qa[G], qb[G];
+  auto flush = [&]() {                         // merge the halves, keep in the unit slot
+    const float m2 = __shfl_xor_sync(kFull, zm, kHalf), s2 = __shfl_xor_sync(kFull, zs, kHalf);
+    lse_merge(zm, zs, m2, s2);
+    if (cur_u >= 0 && half == 0 && head_lane)
+      upart[(warp * kUnitSlots + (cur_u - u_lo)) * G + my_head] = make_float2(zm, zs);
+    zm = -INFINITY;
+    zs = 0.f;
+  };
   bool aborted = false;
   int done = 0;
   for (int i = 0; i < my_count; ++i) {
     const int s = i % STAGES;
-    const bool ok = __all_sync(kFull, mbar_wait_bounded(mybar + s, (i / STAGES) & 1));
-    if (!ok) {
+    const int t0 = 2 * (i * kSelWarps + warp);
+    const int u = int((f_lo + t0) / p.mc);
+    if (u != cur_u) {                          // warp-uniform
+      flush();
+      cur_u = u;
+      const int b = u / p.n_kv_heads, h = u % p.n_kv_heads;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const __nv_bfloat16* qg = p.q + (size_t(b) * (p.n_kv_heads * G) + h * G + g) * kHeadDim;
+        qa[g] = bf16x4_to_f4(*reinterpret_cast<const uint2*>(qg + 4 * hl));
+        qb[g] = bf16x4_to_f4(*reinterpret_cast<const uint2*>(qg + 64 + 4 * hl));
+      }
+    }
+    if (!__all_sync(kFull, mbar_wait_bounded(mybar + s, (i / STAGES) & 1))) {
       if (lane == 0) flag_status(p.status, LOCKS_DEV_WAIT_TIMEOUT);
       aborted = true;
       done = i;
       break;
     }
-    const int j = page_of(i);
-    const int blk = bt[j];
-    float shat[G];
-    if (blk >= 0 && blk < p.num_blocks) {
-      score_page<G, RP, T>(reinterpret_cast<const T*>(myring + size_t(s) * rec_bytes), qv, pbuf,
-                           lane, p.scale, p.scale_log2, shat);
-    } else {
-#pragma unroll
-      for (int g = 0; g < G; ++g) shat[g] = -INFINITY;
-    }
-    // lane g writes head g's score; every lane keeps its head's running LSE
-    float mine = shat[0];
-#pragma unroll
-    for (int g = 1; g < G; ++g)
-      if (lane == g) mine = shat[g];
-    if (lane < G) {
-      ws_s[size_t(j) * G + lane] = mine;
+    const int t = t0 + half;
+    const int blk = s_blk[t];
+    const float shat = score_page16<G, RP, T>(
+        reinterpret_cast<const T*>(myring + size_t(2 * s + half) * rec_bytes), qa, qb, pbuf, hl,
+        p.scale, p.scale_log2);
+    if (head_lane && blk != -2) {
+      const int j = 1 + int((f_lo + t) % p.mc);
+      const int b = u / p.n_kv_heads, h = u % p.n_kv_heads;
+      const float v = blk >= 0 ? shat : -INFINITY;
+      p.ws_scores[(size_t(u) * p.max_pages + j) * G + my_head] = v;
       if (p.page_lse)
-        p.page_lse[(size_t(b) * (p.n_kv_heads * G) + h * G + lane) * p.max_pages + j] = mine;
-      lse_merge(zm, zs, mine, 1.f);
+        p.page_lse[(size_t(b) * (p.n_kv_heads * G) + h * G + my_head) * p.max_pages + j] = v;
+      if (blk >= 0) lse_merge(zm, zs, v, 1.f);
     }
     __syncwarp();
     if (lane == 0 && i + STAGES < my_count) issue(i + STAGES);
@@ -245,92 +315,47 @@ __global__ void __launch_bounds__(kSelThreads)
     for (int i = done; i < min(my_count, done + STAGES); ++i)
       mbar_wait_bounded(mybar + (i % STAGES), (i / STAGES) & 1);
   }
+  flush();
 
-  // ---- chunk partial of log Z -------------------------------------------
-  if (lane < G) wpart[warp * G + lane] = make_float2(zm, zs);
-  __syncthreads();
-  if (tid < G) {
-    float m = -INFINITY, sm = 0.f;
-    for (int w = 0; w < kSelWarps; ++w) {
-      const float2 v = wpart[w * G + tid];
-      lse_merge(m, sm, v.x, v.y);
-    }
-    p.ws_part[(size_t(u) * p.n_chunks_max + chunk) * G + tid] = make_float2(m, sm);
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int ticket = atomicAdd(p.ws_ticket + u, 1);
-    s_is_last = (ticket == nchunks - 1);
-  }
-  __syncthreads();
-  if (!s_is_last) return;
-  __threadfence();
-
-  // ======== last CTA of the unit: normalise, share-average, top-(k-2) =========
-  if (tid < G) {
-    float m = -INFINITY, sm = 0.f;
-    for (int c = 0; c < nchunks; ++c) {
-      const float2 v = __ldcg(p.ws_part + (size_t(u) * p.n_chunks_max + c) * G + tid);
-      lse_merge(m, sm, v.x, v.y);
-    }
-    s_logz[tid] = (sm > 0.f) ? m + logf(sm) : -INFINITY;
-  }
+  // the dependent grid (the finalize kernel) may start launching; it waits for
+  // this grid's completion before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
 
-  const int k = p.k;
-  int32_t* out = p.selected + size_t(u) * k;
-  if (n <= k) {
-    for (int t = tid; t < k; t += kSelThreads) out[t] = t < n ? t : -1;
-    if (tid == 0) p.ws_ticket[u] = 0;
-    // shares are still reported for the candidates
-    for (int idx = tid; idx < n_cand; idx += kSelThreads) {
-      const int j = 1 + idx;
-      float mb = 0.f;
-#pragma unroll
-      for (int g = 0; g < G; ++g) mb += expf(__ldcg(ws_s + size_t(j) * G + g) - s_logz[g]);
-      if (p.page_share) p.page_share[size_t(u) * p.max_pages + j] = mb / G;
-    }
-    return;
+  // write the per-(warp, unit) partials of every unit this CTA touched
+  for (int t = tid; t < kSelWarps * (u_hi - u_lo + 1) * G; t += kSelThreads) {
+    const int g = t % G, w = (t / G) % kSelWarps, us = t / (G * kSelWarps);
+    const int u = u_lo + us;
+    const int i_first = int((long(u) * p.mc) / p.per_cta);
+    const int seg = (int(blockIdx.x) - i_first) * kSelWarps + w;
+    p.ws_part[(size_t(u) * p.nseg_max + seg) * G + g] = upart[(w * kUnitSlots + us) * G + g];
   }
+}
 
-  // the barriers' memory may be reused for the keys below
-  if (lane == 0)
-    for (int s = 0; s < STAGES; ++s)
-      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(mybar + s)) : "memory");
-  __syncthreads();
-  const int K = k - 2;
-  if (K == 0) {
-    if (tid == 0) { out[0] = 0; out[1] = n - 1; p.ws_ticket[u] = 0; }
-    return;
-  }
+// ---------------------------------------------------------------------------
+// block-wide top-K: K largest 32-bit keys, ties to the smaller page id
+// ---------------------------------------------------------------------------
+struct TopkSmem {
+  unsigned int hist[256];
+  unsigned int digit, above;
+  int count, ties;
+};
 
-  // averaged shares as sortable keys (non-negative floats order as their bits)
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-  for (int idx = tid; idx < n_cand; idx += kSelThreads) {
-    const int j = 1 + idx;
-    float mb = 0.f;
-#pragma unroll
-    for (int g = 0; g < G; ++g) mb += expf(__ldcg(ws_s + size_t(j) * G + g) - s_logz[g]);
-    mb *= 1.f / G;
-    keys[idx] = __float_as_uint(mb);
-    if (p.page_share) p.page_share[size_t(u) * p.max_pages + j] = mb;
-  }
-  __syncthreads();
-
-  // radix select of the K-th largest key
-  __shared__ unsigned int hist[256];
-  __shared__ unsigned int s_digit, s_above;
-  __shared__ int scan_scratch[kSelWarps + 1];
+// Threshold of the K-th largest key(i) over i < n with pred(i): returns the
+// key and writes how many elements equal to it must be taken.
+template <int NT, class KeyF, class PredF>
+__device__ uint32_t radix_kth(KeyF key, PredF pred, int n, int K, int* need, TopkSmem& S) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t prefix = 0, mask = 0;
   int kleft = K;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int t = tid; t < 256; t += kSelThreads) hist[t] = 0;
+    for (int t = tid; t < 256; t += NT) S.hist[t] = 0;
     __syncthreads();
-    for (int idx = tid; idx < n_cand; idx += kSelThreads) {
-      const uint32_t key = keys[idx];
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    for (int i = tid; i < n; i += NT) {
+      if (!pred(i)) continue;
+      const uint32_t k = key(i);
+      if ((k & mask) == prefix) atomicAdd(&S.hist[(k >> shift) & 255u], 1u);
     }
     __syncthreads();
     if (warp == 0) {
@@ -338,20 +363,19 @@ __global__ void __launch_bounds__(kSelThreads)
       unsigned int cnt[8], tot = 0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        cnt[e] = hist[8 * (31 - lane) + 7 - e];   // descending bin order
+        cnt[e] = S.hist[8 * (31 - lane) + 7 - e];
         tot += cnt[e];
       }
       const int incl = warp_incl_scan(int(tot), lane);
-      const int excl = incl - int(tot);
       const unsigned int hit = __ballot_sync(kFull, incl >= kleft);
       const int first = __ffs(hit) - 1;
       if (lane == first) {
-        int acc = excl;
+        int acc = incl - int(tot);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           if (acc + int(cnt[e]) >= kleft) {
-            s_digit = 8 * (31 - lane) + 7 - e;
-            s_above = acc;
+            S.digit = 8 * (31 - lane) + 7 - e;
+            S.above = acc;
             break;
           }
           acc += cnt[e];
@@ -359,70 +383,224 @@ __global__ void __launch_bounds__(kSelThreads)
       }
     }
     __syncthreads();
-    prefix |= s_digit << shift;
+    prefix |= S.digit << shift;
     mask |= 255u << shift;
-    kleft -= int(s_above);
+    kleft -= int(S.above);
     __syncthreads();
   }
-  const uint32_t thr = prefix;   // the K-th largest key
-  const int need = kleft;        // keys equal to thr to take (the lowest page ids)
+  *need = kleft;
+  return prefix;
+}
 
-  // collect: contiguous index ranges per thread keep the output ordered
-  const int per = (n_cand + kSelThreads - 1) / kSelThreads;
-  const int lo = min(n_cand, tid * per), hi = min(n_cand, lo + per);
-  int n_eq = 0;
-  for (int idx = lo; idx < hi; ++idx) n_eq += keys[idx] == thr;
-  int tot_eq;
-  const int eq_before = block_excl_scan(n_eq, scan_scratch, &tot_eq);
-  int n_sel = 0;
+// Writes the pages of the K largest keys (ties: smaller page) to out[0..K),
+// unordered.  keys/pages are shared-memory arrays of n >= K entries.
+template <int NT>
+__device__ void block_topk(const uint32_t* keys, const int* pages, int n, int K, int* out,
+                           TopkSmem& S) {
+  const int tid = threadIdx.x;
+  int need;
+  const uint32_t thr = radix_kth<NT>([&](int i) { return keys[i]; }, [](int) { return true; }, n, K,
+                                     &need, S);
+  if (tid == 0) { S.count = 0; S.ties = 0; }
+  __syncthreads();
+  for (int i = tid; i < n; i += NT) {
+    if (keys[i] > thr) out[atomicAdd(&S.count, 1)] = pages[i];
+    else if (keys[i] == thr) atomicAdd(&S.ties, 1);
+  }
+  __syncthreads();
+  const int ties = S.ties;
+  if (ties == need) {
+    for (int i = tid; i < n; i += NT)
+      if (keys[i] == thr) out[atomicAdd(&S.count, 1)] = pages[i];
+  } else {
+    // more equal keys than places: the `need` smallest pages among them
+    int need2;
+    const uint32_t pthr = radix_kth<NT>([&](int i) { return ~uint32_t(pages[i]); },
+                                        [&](int i) { return keys[i] == thr; }, n, need, &need2, S);
+    for (int i = tid; i < n; i += NT)
+      if (keys[i] == thr && ~uint32_t(pages[i]) >= pthr) out[atomicAdd(&S.count, 1)] = pages[i];
+  }
+  __syncthreads();
+}
+
+template <int G>
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  // launched as a programmatic dependent of the score kernel; the decode that
+  // follows may begin launching once every CTA here has started
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int u = blockIdx.y, sl = blockIdx.x;
+  const int b = u / p.n_kv_heads;
+  const int seq_len = unit_seq_len(p, b);
+  if (p.seq_lens[b] > p.max_pages * kPageSize && sl == 0 && tid == 0)
+    flag_status(p.status, LOCKS_DEV_BAD_SEQ_LEN);
+  const int n = (seq_len + kPageSize - 1) / kPageSize;
+  const int n_cand = cand_count(seq_len);
+  const int nsl = max(1, (n_cand + p.slice - 1) / p.slice);
+  if (sl >= nsl) return;
+  const int k = p.k, K = k - 2;
+  int32_t* out = p.selected + size_t(u) * k;
+
+  __shared__ TopkSmem S;
+  __shared__ float s_red[kFinWarps][16][2];
+  __shared__ float s_logz[16];
+  __shared__ int s_is_last;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);       // [slice] / merge keys
+  int* pages = reinterpret_cast<int*>(keys + p.fin_cap);     // [fin_cap]
+  int* win = pages + p.fin_cap;                              // [K]
+
+  // ---- log Z_g from the unit's partials -----------------------------------
   {
-    int e = eq_before;
-    for (int idx = lo; idx < hi; ++idx) {
-      const uint32_t key = keys[idx];
-      if (key > thr) ++n_sel;
-      else if (key == thr) { if (e < need) ++n_sel; ++e; }
+    const int i_first = int((long(u) * p.mc) / p.per_cta);
+    const int i_last = int((long(u + 1) * p.mc - 1) / p.per_cta);
+    const int nseg = (i_last - i_first + 1) * kSelWarps;
+    float m[G], s[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) { m[g] = -INFINITY; s[g] = 0.f; }
+    for (int sg = tid; sg < nseg; sg += kFinThreads) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float2 v = __ldcg(p.ws_part + (size_t(u) * p.nseg_max + sg) * G + g);
+        lse_merge(m[g], s[g], v.x, v.y);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float m2 = __shfl_xor_sync(kFull, m[g], o), s2 = __shfl_xor_sync(kFull, s[g], o);
+        lse_merge(m[g], s[g], m2, s2);
+      }
+      if (lane == 0) { s_red[warp][g][0] = m[g]; s_red[warp][g][1] = s[g]; }
+    }
+    __syncthreads();
+    if (tid < G) {
+      float mm = -INFINITY, ss = 0.f;
+      for (int w = 0; w < kFinWarps; ++w) lse_merge(mm, ss, s_red[w][tid][0], s_red[w][tid][1]);
+      s_logz[tid] = (ss > 0.f) ? mm + logf(ss) : -INFINITY;
+    }
+    __syncthreads();
+  }
+
+  // ---- averaged shares of this slice's candidates ---------------------------
+  const int c_lo = sl * p.slice, c_n = min(n_cand, c_lo + p.slice) - c_lo;
+  const bool select = n > k && K > 0;
+  {
+    float logz[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) logz[g] = s_logz[g];
+    const float* ws_s = p.ws_scores + size_t(u) * p.max_pages * G;
+    constexpr int UNR = 4;
+    for (int base = 0; base < c_n; base += UNR * kFinThreads) {
+      float sv[UNR][G];
+#pragma unroll
+      for (int e = 0; e < UNR; ++e) {
+        const int i = base + e * kFinThreads + tid;
+        if (i < c_n) ld_scores<G>(ws_s + size_t(1 + c_lo + i) * G, sv[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < UNR; ++e) {
+        const int i = base + e * kFinThreads + tid;
+        if (i < c_n) {
+          float mb = 0.f;
+#pragma unroll
+          for (int g = 0; g < G; ++g) mb += expf(sv[e][g] - logz[g]);
+          mb *= 1.f / G;
+          if (select) { keys[i] = __float_as_uint(mb); pages[i] = 1 + c_lo + i; }
+          if (p.page_share) p.page_share[size_t(u) * p.max_pages + 1 + c_lo + i] = mb;
+        }
+      }
     }
   }
-  int tot_sel;
-  int pos = block_excl_scan(n_sel, scan_scratch, &tot_sel);
-  {
-    int e = eq_before;
-    for (int idx = lo; idx < hi; ++idx) {
-      const uint32_t key = keys[idx];
-      bool take = false;
-      if (key > thr) take = true;
-      else if (key == thr) { take = e < need; ++e; }
-      if (take) out[1 + pos++] = 1 + idx;
+  if (!select) {
+    if (sl == 0) {
+      if (n <= k) {
+        for (int t = tid; t < k; t += kFinThreads) out[t] = t < n ? t : -1;
+      } else if (tid == 0) {               // k == 2: the forced pages only
+        out[0] = 0;
+        out[1] = n - 1;
+      }
     }
+    return;
+  }
+  __syncthreads();
+
+  // ---- this slice's top-K -----------------------------------------------------
+  const int Ks = min(K, c_n);
+  block_topk<kFinThreads>(keys, pages, c_n, Ks, win, S);
+  if (nsl > 1) {
+    uint2* cand = p.ws_cand + (size_t(u) * p.nslices_max + sl) * K;
+    for (int t = tid; t < K; t += kFinThreads) {
+      uint2 e = make_uint2(0u, 0xffffffffu);            // empty entry
+      if (t < Ks) e = make_uint2(keys[win[t] - 1 - c_lo], uint32_t(win[t]));
+      cand[t] = e;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_is_last = (atomicAdd(p.ws_ticket + u, 1) == nsl - 1);
+    __syncthreads();
+    if (!s_is_last) return;
+    __threadfence();
+    // merge the slices' winners
+    for (int t = tid; t < nsl * K; t += kFinThreads) {
+      const uint2 e = __ldcg(p.ws_cand + size_t(u) * p.nslices_max * K + t);
+      keys[t] = e.x;
+      pages[t] = int(e.y);                            // empty entries: page -1, key 0
+    }
+    __syncthreads();
+    block_topk<kFinThreads>(keys, pages, nsl * K, K, win, S);
+    if (tid == 0) p.ws_ticket[u] = 0;
+  }
+  // ---- ascending page order ---------------------------------------------------
+  for (int t = tid; t < K; t += kFinThreads) {
+    const int pg = win[t];
+    int r = 0;
+    for (int i = 0; i < K; ++i) r += win[i] < pg;
+    out[1 + r] = pg;
   }
   if (tid == 0) {
     out[0] = 0;
     out[k - 1] = n - 1;
-    p.ws_ticket[u] = 0;   // ready for the next call
   }
 }
 
 template <int G, int RP, typename T>
-int launch_select_t(const SelectParams& p, int grid_x, int grid_y, cudaStream_t stream) {
+int launch_t(const SelectParams& p, int n_score_ctas, int n_slices, cudaStream_t stream) {
   constexpr int STAGES = 2;
-  size_t ring = size_t(kSelWarps) * STAGES * p.rec_bytes;
-  size_t smem = ring + kSelWarps * STAGES * sizeof(uint64_t) +
-                kSelWarps * pbuf_stride<G, RP>() * sizeof(float) + kSelWarps * G * sizeof(float2);
-  const size_t keys = size_t(p.max_pages) * sizeof(uint32_t);
-  if (keys > smem) smem = keys;
-  if (smem > kMaxDynSmem) return LOCKS_ERR_UNSUPPORTED;
-  auto kern = select_kernel<G, RP, T, STAGES>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-      cudaSuccess)
+  const size_t smem = size_t(kSelWarps) * STAGES * 2 * p.rec_bytes +
+                      kSelWarps * STAGES * sizeof(uint64_t) +
+                      kSelWarps * 2 * pbuf_stride<G, RP>() * sizeof(float) +
+                      kSelWarps * kUnitSlots * G * sizeof(float2) + size_t(p.per_cta) * sizeof(int);
+  const size_t fsmem = size_t(p.fin_cap) * 8 + size_t(p.k) * sizeof(int);
+  if (smem > kMaxDynSmem || fsmem > kMaxDynSmem) return LOCKS_ERR_UNSUPPORTED;
+  auto sk = score_kernel<G, RP, T, STAGES>;
+  auto fk = finalize_kernel<G>;
+  if (cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, int(fsmem)) !=
+          cudaSuccess)
     return LOCKS_ERR_CUDA;
-  kern<<<dim3(grid_x, grid_y), kSelThreads, smem, stream>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
+  sk<<<n_score_ctas, kSelThreads, smem, stream>>>(p);
+  if (cudaPeekAtLastError() != cudaSuccess) return LOCKS_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(n_slices, p.units);
+  lc.blockDim = dim3(kFinThreads);
+  lc.dynamicSmemBytes = fsmem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, fk, p) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
 }
 
 template <typename T>
-int dispatch_g(const SelectParams& p, int G, int RP, int gx, int gy, cudaStream_t s) {
-#define LOCKS_SEL_CASE(GG, RR)                                \
-  if (G == GG && RP == RR) return launch_select_t<GG, RR, T>(p, gx, gy, s);
+int dispatch(const SelectParams& p, int G, int RP, int nsc, int nsl, cudaStream_t s) {
+#define LOCKS_SEL_CASE(GG, RR) \
+  if (G == GG && RP == RR) return launch_t<GG, RR, T>(p, nsc, nsl, s);
   LOCKS_SEL_CASE(1, 4) LOCKS_SEL_CASE(1, 8) LOCKS_SEL_CASE(1, 16)
   LOCKS_SEL_CASE(2, 4) LOCKS_SEL_CASE(2, 8) LOCKS_SEL_CASE(2, 16)
   LOCKS_SEL_CASE(4, 4) LOCKS_SEL_CASE(4, 8) LOCKS_SEL_CASE(4, 16)
@@ -431,18 +609,44 @@ int dispatch_g(const SelectParams& p, int G, int RP, int gx, int gy, cudaStream_
   return LOCKS_ERR_UNSUPPORTED;
 }
 
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
 }  // namespace
 
-int select_chunk_pages(int max_pages) {
-  // candidates per CTA: enough chunks for several waves, at least 2 pages/warp
-  (void)max_pages;
-  return 8 * kSelWarps;
+SelectGeom select_geometry(int units, int max_pages, int G, int k) {
+  SelectGeom g;
+  const int K = k > 2 ? k - 2 : 1;
+  g.mc = (max_pages > 2 ? max_pages - 2 : 1);
+  g.mc += g.mc & 1;                                   // even: page pairs never straddle units
+  const long total = long(units) * g.mc;
+  // about two CTAs per SM on 152 SMs, at least 16 slots each, a CTA spanning
+  // at most kUnitSlots units, and the slot ids of one CTA in shared memory
+  long per = (total + 2 * 152 - 1) / (2 * 152);
+  per += per & 1;
+  if (per < 16) per = 16;
+  if (per > 2048) per = 2048;
+  const long cap = long(kUnitSlots - 2) * g.mc;
+  if (per > cap) per = cap & ~1L;
+  g.per_cta = int(per);
+  g.n_score_ctas = int(total > 0 ? (total + per - 1) / per : 1);
+  g.nseg_max = ((g.mc + g.per_cta - 1) / g.per_cta + 1) * kSelWarps;
+  g.slice = 2048;
+  g.nslices_max = (g.mc + g.slice - 1) / g.slice;
+  if (g.nslices_max < 1) g.nslices_max = 1;
+  g.fin_cap = g.slice > g.nslices_max * K ? g.slice : g.nslices_max * K;
+  const size_t U = size_t(units);
+  g.off_scores = 0;
+  g.off_part = align256(U * max_pages * G * sizeof(float));
+  g.off_cand = g.off_part + align256(U * g.nseg_max * G * sizeof(float2));
+  g.off_ticket = g.off_cand + align256(U * g.nslices_max * K * sizeof(uint2));
+  g.total = g.off_ticket + align256(U * sizeof(int32_t));
+  return g;
 }
 
-int launch_select(const SelectParams& p, int G, int RP, int dtype, int grid_x, int grid_y,
-                  cudaStream_t stream) {
-  if (dtype == LOCKS_SUMMARY_F32) return dispatch_g<float>(p, G, RP, grid_x, grid_y, stream);
-  return dispatch_g<__nv_bfloat16>(p, G, RP, grid_x, grid_y, stream);
+int launch_select(const SelectParams& p, int G, int RP, int dtype, int n_score_ctas,
+                  int n_slices, cudaStream_t stream) {
+  if (dtype == LOCKS_SUMMARY_F32) return dispatch<float>(p, G, RP, n_score_ctas, n_slices, stream);
+  return dispatch<__nv_bfloat16>(p, G, RP, n_score_ctas, n_slices, stream);
 }
 
 }  // namespace locks
