@@ -188,6 +188,7 @@ int locks_select(const locks_cfg_t* cfg, const void* q, const void* summaries,
   p.slice = L.slice;
   p.nslices_max = L.nslices_max;
   p.fin_cap = L.fin_cap;
+  p.cand_per_slice = L.cand_per_slice;
   p.scale = float(1.0 / std::sqrt(double(cfg->head_dim)));
   p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(cfg->head_dim)));
   return locks::launch_select(p, group_of(cfg), locks::rank_cap(cfg->rank), cfg->summary_dtype,

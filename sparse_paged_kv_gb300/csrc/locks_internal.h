@@ -24,13 +24,13 @@ struct SelectParams {
   int32_t* status;               // nullable
   float* ws_scores;              // [U][max_pages][G]
   float2* ws_part;               // [U][nseg_max][G] log-sum-exp partials
-  uint2* ws_cand;                // [U][nslices_max][k-2] slice winners (key, page)
+  uint2* ws_cand;                // [U][nslices_max][cand_per_slice] slice winners
   int32_t* ws_ticket;            // [U]
   size_t rec_bytes;
   int units, n_kv_heads, max_pages, num_blocks;
   int k;                         // page budget
   int mc, per_cta, nseg_max;     // score kernel geometry (see select_geometry)
-  int slice, nslices_max, fin_cap;
+  int slice, nslices_max, fin_cap, cand_per_slice;
   float scale, scale_log2;
 };
 
@@ -44,6 +44,7 @@ struct SelectGeom {
   int slice;         // candidates per finalize CTA
   int nslices_max;
   int fin_cap;       // finalize shared-memory entries
+  int cand_per_slice;
   size_t off_scores, off_part, off_cand, off_ticket, total;
 };
 

@@ -333,94 +333,163 @@ __global__ void __launch_bounds__(kSelThreads, (G >= 8 || G * RP >= 64 || sizeof
 }
 
 // ---------------------------------------------------------------------------
-// block-wide top-K: K largest 32-bit keys, ties to the smaller page id
+// register sorting networks over 32 lanes (64-bit keys, descending)
 // ---------------------------------------------------------------------------
-struct TopkSmem {
-  unsigned int hist[256];
-  unsigned int digit, above;
-  int count, ties;
-};
-
-// Threshold of the K-th largest key(i) over i < n with pred(i): returns the
-// key and writes how many elements equal to it must be taken.
-template <int NT, class KeyF, class PredF>
-__device__ uint32_t radix_kth(KeyF key, PredF pred, int n, int K, int* need, TopkSmem& S) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0, mask = 0;
-  int kleft = K;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int t = tid; t < 256; t += NT) S.hist[t] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += NT) {
-      if (!pred(i)) continue;
-      const uint32_t k = key(i);
-      if ((k & mask) == prefix) atomicAdd(&S.hist[(k >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins [8*(31-l), 8*(31-l)+8): lane 0 the highest
-      unsigned int cnt[8], tot = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        cnt[e] = S.hist[8 * (31 - lane) + 7 - e];
-        tot += cnt[e];
-      }
-      const int incl = warp_incl_scan(int(tot), lane);
-      const unsigned int hit = __ballot_sync(kFull, incl >= kleft);
-      const int first = __ffs(hit) - 1;
-      if (lane == first) {
-        int acc = incl - int(tot);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (acc + int(cnt[e]) >= kleft) {
-            S.digit = 8 * (31 - lane) + 7 - e;
-            S.above = acc;
-            break;
-          }
-          acc += cnt[e];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= S.digit << shift;
-    mask |= 255u << shift;
-    kleft -= int(S.above);
-    __syncthreads();
-  }
-  *need = kleft;
-  return prefix;
+// Composite key of a candidate: share bits above the inverted page id, so a
+// larger key is a larger share and, between equal shares, a smaller page.
+__device__ __forceinline__ unsigned long long cand_key(uint32_t share_bits, uint32_t page) {
+  return (static_cast<unsigned long long>(share_bits) << 32) | (0xffffffffu - page);
+}
+__device__ __forceinline__ uint32_t key_page(unsigned long long k) {
+  return 0xffffffffu - static_cast<uint32_t>(k);
 }
 
-// Writes the pages of the K largest keys (ties: smaller page) to out[0..K),
-// unordered.  keys/pages are shared-memory arrays of n >= K entries.
-template <int NT>
-__device__ void block_topk(const uint32_t* keys, const int* pages, int n, int K, int* out,
-                           TopkSmem& S) {
-  const int tid = threadIdx.x;
-  int need;
-  const uint32_t thr = radix_kth<NT>([&](int i) { return keys[i]; }, [](int) { return true; }, n, K,
-                                     &need, S);
-  if (tid == 0) { S.count = 0; S.ties = 0; }
-  __syncthreads();
-  for (int i = tid; i < n; i += NT) {
-    if (keys[i] > thr) out[atomicAdd(&S.count, 1)] = pages[i];
-    else if (keys[i] == thr) atomicAdd(&S.ties, 1);
+__device__ __forceinline__ unsigned long long shfl_xor64(unsigned long long v, int m) {
+  return __shfl_xor_sync(kFull, v, m);
+}
+
+// Bitonic sort of one value per lane across the warp, descending in lane order.
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long o = shfl_xor64(v, j);
+      const bool lower = (lane & j) == 0, first_half = (lane & k) == 0 || k == 32;
+      v = (lower == first_half) ? (v > o ? v : o) : (v < o ? v : o);
+    }
   }
-  __syncthreads();
-  const int ties = S.ties;
-  if (ties == need) {
-    for (int i = tid; i < n; i += NT)
-      if (keys[i] == thr) out[atomicAdd(&S.count, 1)] = pages[i];
-  } else {
-    // more equal keys than places: the `need` smallest pages among them
-    int need2;
-    const uint32_t pthr = radix_kth<NT>([&](int i) { return ~uint32_t(pages[i]); },
-                                        [&](int i) { return keys[i] == thr; }, n, need, &need2, S);
-    for (int i = tid; i < n; i += NT)
-      if (keys[i] == thr && ~uint32_t(pages[i]) >= pthr) out[atomicAdd(&S.count, 1)] = pages[i];
+  return v;
+}
+
+// Given a bitonic sequence across the lanes, sort it descending.
+__device__ __forceinline__ unsigned long long warp_bitonic_merge_desc(unsigned long long v,
+                                                                     int lane) {
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const unsigned long long o = shfl_xor64(v, j);
+    v = ((lane & j) == 0) ? (v > o ? v : o) : (v < o ? v : o);
   }
-  __syncthreads();
+  return v;
+}
+
+// Top 32 of two descending lane-ordered lists, descending.
+__device__ __forceinline__ unsigned long long warp_merge_top32(unsigned long long a,
+                                                              unsigned long long b, int lane) {
+  const unsigned long long br = __shfl_sync(kFull, b, 31 - lane);
+  return warp_bitonic_merge_desc(a > br ? a : br, lane);
+}
+
+// Sorts each of the 8 per-lane columns and merges them: returns the warp's
+// top 32 of its 256 keys, descending in lane order.
+__device__ __forceinline__ unsigned long long warp_top32_of_256(unsigned long long (&v)[8],
+                                                               int lane) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] = warp_sort_desc(v[e], lane);
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) v[e] = warp_merge_top32(v[e], v[e + 1], lane);
+#pragma unroll
+  for (int e = 0; e < 8; e += 4) v[e] = warp_merge_top32(v[e], v[e + 2], lane);
+  return warp_merge_top32(v[0], v[4], lane);
+}
+
+// Writes the first K (<= 32) keys of a descending list as pages in increasing
+// page order to out[0..K).
+__device__ __forceinline__ void warp_emit_pages_ascending(unsigned long long top, int K,
+                                                          int32_t* out, int lane) {
+  // sort the chosen pages ascending: key = inverted page (descending sort),
+  // lanes beyond K get the smallest key
+  unsigned long long pk = lane < K ? static_cast<unsigned long long>(0xffffffffu - key_page(top))
+                                   : 0ull;
+  pk = warp_sort_desc(pk, lane);
+  if (lane < K) out[lane] = int32_t(0xffffffffu - static_cast<uint32_t>(pk));
+}
+
+// ---------------------------------------------------------------------------
+// warp-level top-K over a list kept in increasing page order
+// ---------------------------------------------------------------------------
+// Chooses the K largest keys of list[0, m) (shared memory, entries in
+// increasing page order) with one warp: a 4-pass 8-bit radix select of the
+// K-th largest key in a private 256-bin histogram, then the entries above it
+// and, among the entries equal to it, the earliest (smaller pages).  The
+// chosen entries are written in list order -- still increasing page order --
+// to out_keys / out_pages; returns their number, min(K, m).
+__device__ int warp_topk(const uint32_t* keys, const int* pages, int m, int K, uint32_t* out_keys,
+                         int* out_pages, unsigned* hist) {
+  const int lane = threadIdx.x & 31;
+  if (m <= K) {
+    for (int i = lane; i < m; i += 32) { out_keys[i] = keys[i]; out_pages[i] = pages[i]; }
+    __syncwarp();
+    return m;
+  }
+  // lane l looks at entries l, l + 32, l + 64, ... (conflict-free shared loads)
+  uint32_t prefix = 0, mask = 0;
+  int kleft = K;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hist[e * 32 + lane] = 0;
+    __syncwarp();
+    for (int i0 = 0; i0 < m; i0 += 32) {
+      // one atomic per distinct bin per round (keys crowd into a few bins)
+      const int i = i0 + lane;
+      uint32_t bin = 256u;                     // not counted
+      if (i < m) {
+        const uint32_t k = keys[i];
+        if ((k & mask) == prefix) bin = (k >> shift) & 255u;
+      }
+      const unsigned peers = __match_any_sync(kFull, bin);
+      if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], unsigned(__popc(peers)));
+    }
+    __syncwarp();
+    // lane l owns bins [8*(31-l), 8*(31-l)+8): lane 0 the highest
+    unsigned cnt[8], tot = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      cnt[e] = hist[8 * (31 - lane) + 7 - e];
+      tot += cnt[e];
+    }
+    const int incl = warp_incl_scan(int(tot), lane);
+    const int first = __ffs(__ballot_sync(kFull, incl >= kleft)) - 1;
+    int digit = 0, above = 0;
+    if (lane == first) {
+      int acc = incl - int(tot);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (acc + int(cnt[e]) >= kleft) { digit = 8 * (31 - lane) + 7 - e; above = acc; break; }
+        acc += cnt[e];
+      }
+    }
+    digit = __shfl_sync(kFull, digit, first);
+    above = __shfl_sync(kFull, above, first);
+    prefix |= uint32_t(digit) << shift;
+    mask |= 255u << shift;
+    kleft -= above;
+    __syncwarp();
+  }
+  const uint32_t thr = prefix;
+  const int need = kleft;                     // entries equal to thr to take
+  // collect in list order, 32 entries per round: ballots give the positions
+  const unsigned lt = (1u << lane) - 1;
+  int pos = 0, eq_seen = 0;
+  for (int i0 = 0; i0 < m; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t k = i < m ? keys[i] : 0u;
+    const bool eq = i < m && k == thr;
+    const unsigned eq_bal = __ballot_sync(kFull, eq);
+    const bool take = (i < m && k > thr) || (eq && eq_seen + __popc(eq_bal & lt) < need);
+    const unsigned tb = __ballot_sync(kFull, take);
+    if (take) {
+      const int at = pos + __popc(tb & lt);
+      out_keys[at] = k;
+      out_pages[at] = pages[i];
+    }
+    pos += __popc(tb);
+    eq_seen += __popc(eq_bal);
+  }
+  __syncwarp();
+  return K;
 }
 
 template <int G>
@@ -443,19 +512,24 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   const int k = p.k, K = k - 2;
   int32_t* out = p.selected + size_t(u) * k;
 
-  __shared__ TopkSmem S;
   __shared__ float s_red[kFinWarps][16][2];
   __shared__ float s_logz[16];
+  __shared__ int s_cnt[kFinWarps];
   __shared__ int s_is_last;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);       // [slice] / merge keys
-  int* pages = reinterpret_cast<int*>(keys + p.fin_cap);     // [fin_cap]
-  int* win = pages + p.fin_cap;                              // [K]
+  // shared memory: keys[cap] pages[cap] | warp winners wk/wp [8][K] | list lk/lp [8K] | hist [8][256]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+  int* pages = reinterpret_cast<int*>(keys + p.fin_cap);
+  uint32_t* wk = reinterpret_cast<uint32_t*>(pages + p.fin_cap);
+  int* wp = reinterpret_cast<int*>(wk + kFinWarps * K);
+  uint32_t* lk = reinterpret_cast<uint32_t*>(wp + kFinWarps * K);
+  int* lp = reinterpret_cast<int*>(lk + kFinWarps * K);
+  unsigned* hist = reinterpret_cast<unsigned*>(lp + kFinWarps * K) + warp * 256;
 
   // ---- log Z_g from the unit's partials -----------------------------------
   {
     const int i_first = int((long(u) * p.mc) / p.per_cta);
     const int i_last = int((long(u + 1) * p.mc - 1) / p.per_cta);
-    const int nseg = (i_last - i_first + 1) * kSelWarps;
+    const int nseg = (i_last - i_first + 1) * 4;
     float m[G], s[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) { m[g] = -INFINITY; s[g] = 0.f; }
@@ -485,24 +559,87 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   }
 
   // ---- averaged shares of this slice's candidates ---------------------------
+  // warp w owns entries [256w, 256w + 256) of the slice, lane l every 32nd
   const int c_lo = sl * p.slice, c_n = min(n_cand, c_lo + p.slice) - c_lo;
   const bool select = n > k && K > 0;
+  const float* ws_s = p.ws_scores + size_t(u) * p.max_pages * G;
+  if (select && K <= 32) {
+    // ---- register path: sorting networks, no shared-memory passes -------------
+    __shared__ unsigned long long s_top[kFinWarps][32];
+    unsigned long long v[8];
+    {
+      float sv[8][G];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = warp * 256 + 32 * e + lane;
+        if (i < c_n) ld_scores<G>(ws_s + size_t(1 + c_lo + i) * G, sv[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = warp * 256 + 32 * e + lane;
+        v[e] = 0ull;                                   // below every real candidate
+        if (i < c_n) {
+          float mb = 0.f;
+#pragma unroll
+          for (int g = 0; g < G; ++g) mb += expf(sv[e][g] - s_logz[g]);
+          mb *= 1.f / G;
+          v[e] = cand_key(__float_as_uint(mb), uint32_t(1 + c_lo + i));
+          if (p.page_share) p.page_share[size_t(u) * p.max_pages + 1 + c_lo + i] = mb;
+        }
+      }
+    }
+    s_top[warp][lane] = warp_top32_of_256(v, lane);
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long t[kFinWarps];
+#pragma unroll
+      for (int w = 0; w < kFinWarps; ++w) t[w] = s_top[w][lane];
+#pragma unroll
+      for (int w = 0; w < kFinWarps; w += 2) t[w] = warp_merge_top32(t[w], t[w + 1], lane);
+#pragma unroll
+      for (int w = 0; w < kFinWarps; w += 4) t[w] = warp_merge_top32(t[w], t[w + 2], lane);
+      t[0] = warp_merge_top32(t[0], t[4], lane);
+      if (nsl == 1) {
+        warp_emit_pages_ascending(t[0], K, out + 1, lane);
+        if (lane == 0) { out[0] = 0; out[k - 1] = n - 1; }
+      } else {
+        uint2* cand = p.ws_cand + (size_t(u) * p.nslices_max + sl) * p.cand_per_slice;
+        cand[lane] = make_uint2(uint32_t(t[0] >> 32), uint32_t(t[0]));
+      }
+    }
+    if (nsl == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_is_last = (atomicAdd(p.ws_ticket + u, 1) == nsl - 1);
+    __syncthreads();
+    if (!s_is_last) return;
+    __threadfence();
+    if (warp == 0) {
+      unsigned long long acc = 0ull;
+      for (int s2 = 0; s2 < nsl; ++s2) {
+        const uint2 e = __ldcg(p.ws_cand + (size_t(u) * p.nslices_max + s2) * p.cand_per_slice + lane);
+        const unsigned long long x = (static_cast<unsigned long long>(e.x) << 32) | e.y;
+        acc = s2 == 0 ? x : warp_merge_top32(acc, x, lane);
+      }
+      warp_emit_pages_ascending(acc, K, out + 1, lane);
+      if (lane == 0) { out[0] = 0; out[k - 1] = n - 1; p.ws_ticket[u] = 0; }
+    }
+    return;
+  }
   {
     float logz[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) logz[g] = s_logz[g];
-    const float* ws_s = p.ws_scores + size_t(u) * p.max_pages * G;
-    constexpr int UNR = 4;
-    for (int base = 0; base < c_n; base += UNR * kFinThreads) {
-      float sv[UNR][G];
+    constexpr int PER = 8;
+    for (int base = 0; base < c_n; base += PER * kFinThreads) {
+      const int i0 = base + warp * 32 * PER + lane;
+      float sv[PER][G];
 #pragma unroll
-      for (int e = 0; e < UNR; ++e) {
-        const int i = base + e * kFinThreads + tid;
-        if (i < c_n) ld_scores<G>(ws_s + size_t(1 + c_lo + i) * G, sv[e]);
-      }
+      for (int e = 0; e < PER; ++e)
+        if (i0 + 32 * e < c_n) ld_scores<G>(ws_s + size_t(1 + c_lo + i0 + 32 * e) * G, sv[e]);
 #pragma unroll
-      for (int e = 0; e < UNR; ++e) {
-        const int i = base + e * kFinThreads + tid;
+      for (int e = 0; e < PER; ++e) {
+        const int i = i0 + 32 * e;
         if (i < c_n) {
           float mb = 0.f;
 #pragma unroll
@@ -527,42 +664,64 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   }
   __syncthreads();
 
-  // ---- this slice's top-K -----------------------------------------------------
-  const int Ks = min(K, c_n);
-  block_topk<kFinThreads>(keys, pages, c_n, Ks, win, S);
-  if (nsl > 1) {
-    uint2* cand = p.ws_cand + (size_t(u) * p.nslices_max + sl) * K;
-    for (int t = tid; t < K; t += kFinThreads) {
-      uint2 e = make_uint2(0u, 0xffffffffu);            // empty entry
-      if (t < Ks) e = make_uint2(keys[win[t] - 1 - c_lo], uint32_t(win[t]));
-      cand[t] = e;
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_is_last = (atomicAdd(p.ws_ticket + u, 1) == nsl - 1);
-    __syncthreads();
-    if (!s_is_last) return;
-    __threadfence();
-    // merge the slices' winners
-    for (int t = tid; t < nsl * K; t += kFinThreads) {
-      const uint2 e = __ldcg(p.ws_cand + size_t(u) * p.nslices_max * K + t);
-      keys[t] = e.x;
-      pages[t] = int(e.y);                            // empty entries: page -1, key 0
-    }
-    __syncthreads();
-    block_topk<kFinThreads>(keys, pages, nsl * K, K, win, S);
-    if (tid == 0) p.ws_ticket[u] = 0;
+  // ---- this slice's top-K: per warp over 256 entries, then warp 0 merges ------
+  {
+    const int w_lo = warp * 256, w_m = max(0, min(c_n - w_lo, 256));
+    const int c = warp_topk(keys + w_lo, pages + w_lo, w_m, K, wk + warp * K, wp + warp * K, hist);
+    if (lane == 0) s_cnt[warp] = c;
   }
-  // ---- ascending page order ---------------------------------------------------
-  for (int t = tid; t < K; t += kFinThreads) {
-    const int pg = win[t];
-    int r = 0;
-    for (int i = 0; i < K; ++i) r += win[i] < pg;
-    out[1 + r] = pg;
+  __syncthreads();
+  if (warp == 0) {
+    // concatenate the warp winners in warp order (page order is kept)
+    int off = 0;
+    for (int w = 0; w < kFinWarps; ++w) {
+      const int c = s_cnt[w];
+      for (int i = lane; i < c; i += 32) { lk[off + i] = wk[w * K + i]; lp[off + i] = wp[w * K + i]; }
+      off += c;
+    }
+    __syncwarp();
+    const int got = warp_topk(lk, lp, off, K, wk, wp, hist);
+    if (nsl == 1) {
+      for (int i = lane; i < K; i += 32) out[1 + i] = wp[i];   // increasing page order
+      if (lane == 0) { out[0] = 0; out[k - 1] = n - 1; }
+    } else {
+      uint2* cand = p.ws_cand + (size_t(u) * p.nslices_max + sl) * p.cand_per_slice;
+      for (int i = lane; i < K; i += 32)
+        cand[i] = i < got ? make_uint2(wk[i], uint32_t(wp[i])) : make_uint2(0u, 0xffffffffu);
+    }
   }
-  if (tid == 0) {
-    out[0] = 0;
-    out[k - 1] = n - 1;
+  if (nsl == 1) return;
+
+  // ---- several slices: the last one merges the slices' winners ---------------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_is_last = (atomicAdd(p.ws_ticket + u, 1) == nsl - 1);
+  __syncthreads();
+  if (!s_is_last) return;
+  __threadfence();
+  if (warp == 0) {
+    // slices in order, each in page order, empty entries (page -1) dropped
+    int off = 0;
+    for (int s2 = 0; s2 < nsl; ++s2) {
+      const uint2* src = p.ws_cand + (size_t(u) * p.nslices_max + s2) * p.cand_per_slice;
+      for (int i0 = 0; i0 < K; i0 += 32) {
+        const int i = i0 + lane;
+        uint2 e = make_uint2(0u, 0xffffffffu);
+        if (i < K) e = __ldcg(src + i);
+        const bool ok = i < K && e.y != 0xffffffffu;
+        const unsigned bal = __ballot_sync(kFull, ok);
+        if (ok) {
+          const int at = off + __popc(bal & ((1u << lane) - 1));
+          keys[at] = e.x;
+          pages[at] = int(e.y);
+        }
+        off += __popc(bal);
+      }
+    }
+    __syncwarp();
+    warp_topk(keys, pages, off, K, wk, wp, hist);
+    for (int i = lane; i < K; i += 32) out[1 + i] = wp[i];
+    if (lane == 0) { out[0] = 0; out[k - 1] = n - 1; p.ws_ticket[u] = 0; }
   }
 }
 
@@ -573,7 +732,9 @@ int launch_t(const SelectParams& p, int n_score_ctas, int n_slices, cudaStream_t
                       kSelWarps * STAGES * sizeof(uint64_t) +
                       kSelWarps * 2 * pbuf_stride<G, RP>() * sizeof(float) +
                       kSelWarps * kUnitSlots * G * sizeof(float2) + size_t(p.per_cta) * sizeof(int);
-  const size_t fsmem = size_t(p.fin_cap) * 8 + size_t(p.k) * sizeof(int);
+  const int K = p.k > 2 ? p.k - 2 : 1;
+  const size_t fsmem = size_t(p.fin_cap) * 8 + size_t(kFinWarps) * K * 8 * 2 +
+                       size_t(kFinWarps) * 256 * sizeof(unsigned);
   if (smem > kMaxDynSmem || fsmem > kMaxDynSmem) return LOCKS_ERR_UNSUPPORTED;
   auto sk = score_kernel<G, RP, T, STAGES>;
   auto fk = finalize_kernel<G>;
@@ -633,12 +794,13 @@ SelectGeom select_geometry(int units, int max_pages, int G, int k) {
   g.slice = 2048;
   g.nslices_max = (g.mc + g.slice - 1) / g.slice;
   if (g.nslices_max < 1) g.nslices_max = 1;
+  g.cand_per_slice = K > 32 ? K : 32;
   g.fin_cap = g.slice > g.nslices_max * K ? g.slice : g.nslices_max * K;
   const size_t U = size_t(units);
   g.off_scores = 0;
   g.off_part = align256(U * max_pages * G * sizeof(float));
   g.off_cand = g.off_part + align256(U * g.nseg_max * G * sizeof(float2));
-  g.off_ticket = g.off_cand + align256(U * g.nslices_max * K * sizeof(uint2));
+  g.off_ticket = g.off_cand + align256(U * g.nslices_max * g.cand_per_slice * sizeof(uint2));
   g.total = g.off_ticket + align256(U * sizeof(int32_t));
   return g;
 }

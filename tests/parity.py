@@ -7,7 +7,10 @@ Gates (fp32 summaries, bf16 KV with fp32 accumulation):
   * attention outputs: 2e-2 absolute (bf16 output), lse 1e-3 absolute; the
     sparse output is compared with the oracle attending the GPU's selected set,
     so a legitimate tie-window difference cannot fail it;
-  * build: the projector-invariant reconstruction C V^T within 1e-4 of max|D|,
+  * build: the projector-invariant reconstruction C V^T within
+    max(1e-4, 2e-5 * sigma_1^2 / (sigma_r^2 - sigma_{r+1}^2)) of max|D| -- the
+    rank-r subspace is fixed only up to the spectral gap (Cor. 1), and an fp32
+    solve perturbs it by about (fp32 roundoff x sigma_1^2) / gap (Davis-Kahan) --
     the top-r sigma^2 (= squared column norms of C) within 1e-4 of sigma_1^2,
     V^T V = I within 1e-4, tau within 1e-4 of the Gram trace.
 Pages whose relative spectral gap (sigma_r^2 - sigma_{r+1}^2) / sigma_1^2 is
@@ -28,6 +31,7 @@ OUT_TOL = 2e-2
 OUT_LSE_TOL = 1e-3
 TIE_TOL = 1e-5
 RECON_TOL = 1e-4
+RECON_GAP_COEF = 2e-5
 SIGMA_TOL = 1e-4
 ORTHO_TOL = 1e-4
 TAU_TOL = 1e-4
@@ -113,8 +117,10 @@ def compare_build(layer, inputs, res: O.UnitResult, rep: Report, tail=None, stat
         rec_ref = s.C @ s.V.T
         e_rec = np.abs(rec_gpu - rec_ref).max() / scale
         rep.max_recon_rel = max(rep.max_recon_rel, e_rec)
-        if e_rec > RECON_TOL:
-            rep.fail(f"reconstruction b{b} h{h} p{j}: {e_rec:.2e}")
+        gap = (s.sigma2[r - 1] - s.sigma2[r]) / s.sigma2[0] if len(s.sigma2) > r else 1.0
+        tol = max(RECON_TOL, RECON_GAP_COEF / gap)
+        if e_rec > tol:
+            rep.fail(f"reconstruction b{b} h{h} p{j}: {e_rec:.2e} (relative gap {gap:.2e})")
         if tail is not None and block_index is not None:
             t_gpu = float(tail[block_index[blocks[n_]], h])
             trace = float(np.trace(D @ D.T))

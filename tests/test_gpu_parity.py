@@ -26,6 +26,13 @@ CASES = {
                              carrier_frac=0.01, budget_tokens=2048, seed=2009),
     "batch_heads": TINY.with_(batch=3, n_q_heads=16, n_kv_heads=4, context=64 * 70,
                               global_rank=16, seed=2010),
+    # more than 2048 candidates: several finalize slices, merged by the last one
+    "slices3": TINY.with_(context=64 * 4200 + 11, global_rank=16, carrier_count=None,
+                          carrier_frac=0.01, budget_tokens=2048, seed=2014),
+    # k - 2 > 32: the radix top-k path, with one and with several slices
+    "k40": TINY.with_(context=64 * 300, budget_tokens=64 * 40, seed=2015),
+    "k40_slices3": TINY.with_(context=64 * 4200, budget_tokens=64 * 40, global_rank=16,
+                              seed=2016),
 }
 
 
