@@ -157,6 +157,29 @@ def profile_traffic(kernel_key: str, config: str):
 
 
 # --------------------------------------------------------------------------
+# replicas across ranks (weak scaling: every rank runs its own batch)
+# --------------------------------------------------------------------------
+def replica_workload(w, rank: int):
+    """Rank r's replica of workload w: same shapes, its own seed."""
+    return w.with_(seed=w.seed + 7919 * rank) if rank else w
+
+
+def reduce_max(value: float, dist=None, device="cpu") -> float:
+    """Maximum of a per-rank value over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tokens_per_s(world: int, batch: int, step_ms_max: float) -> float:
+    """Whole-job throughput: every rank's batch per step over the slowest rank's step."""
+    return world * batch / (step_ms_max / 1e3)
+
+
+# --------------------------------------------------------------------------
 # CPU baseline: the oracle, in a fresh single-threaded process
 # --------------------------------------------------------------------------
 def cpu_worker(spec: str):
@@ -288,9 +311,7 @@ def run_gpu(args):
 
     build_lib.build()
     Bd.load_library()
-    w = W.get(args.config)
-    if world > 1:
-        w = w.with_(seed=w.seed + 7919 * rank)
+    w = replica_workload(W.get(args.config), rank)
     t0 = time.time()
     inputs = W.generate(w)
     gen_s = time.time() - t0
@@ -376,12 +397,7 @@ def run_gpu(args):
     select_bytes, decode_bytes, dense_bytes = algorithmic_bytes(layer, inputs, selected)
 
     mean_step = sum(step_ms) / K
-    if dist:
-        t = torch.tensor([mean_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_step_max = float(t.item())
-    else:
-        mean_step_max = mean_step
+    mean_step_max = reduce_max(mean_step, dist, "cuda")
 
     # ---- dense comparison ----
     dense = None
@@ -414,12 +430,8 @@ def run_gpu(args):
             if ev:
                 ev[1].record(stream)
         eevs, _ = timed(estep, K, Wm, marks=2)
-        ems = sum(e[0].elapsed_time(e[1]) for e in eevs) / K
-        if dist:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * w.batch / (ems / 1e3), "unit": "tokens/s",
+        ems = reduce_max(sum(e[0].elapsed_time(e[1]) for e in eevs) / K, dist, "cuda")
+        e2e = {"value": aggregate_tokens_per_s(world, w.batch, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
                "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
                "us_per_step": ems * 1e3}
@@ -438,7 +450,7 @@ def run_gpu(args):
     step_gbs = (select_bytes + decode_bytes) / (mean_step / 1e3) / 1e9
     line = {
         "metric": METRIC,
-        "value": world * w.batch / (mean_step_max / 1e3),
+        "value": aggregate_tokens_per_s(world, w.batch, mean_step_max),
         "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": mean_step_max,
