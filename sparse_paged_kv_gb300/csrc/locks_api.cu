@@ -3,6 +3,9 @@
 // allocates, frees or synchronises.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "locks_common.cuh"
 #include "locks_internal.h"
@@ -49,17 +52,43 @@ DecodeLayout decode_layout(const locks_cfg_t* c, int n_pages) {
   DecodeLayout L;
   const int G = group_of(c);
   const size_t U = size_t(c->batch) * c->n_kv_heads;
-  // aim for about three waves of two CTAs per SM on 152 SMs
-  const double total_pages = double(U) * (n_pages > 0 ? n_pages : 1);
-  int pps = int(std::ceil(total_pages / (152.0 * 2.0 * 3.0)));
-  if (pps < 1) pps = 1;
-  if (pps > 64) pps = 64;
-  L.pages_per_split = pps;
-  L.n_splits_max = n_pages > 0 ? (n_pages + pps - 1) / pps : 1;
+  L.pages_per_split = locks::decode_pages_per_split(long(U), n_pages);
+  L.n_splits_max = n_pages > 0 ? (n_pages + L.pages_per_split - 1) / L.pages_per_split : 1;
   L.part = 0;
   L.ticket = align_up(U * L.n_splits_max * G * locks::kPartStride * sizeof(float));
   L.total = L.ticket + align_up(U * sizeof(int32_t));
   return L;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// A KV pool viewed as a 2-D bf16 tensor of (num_blocks * n_kv_heads * B) rows
+// of head_dim elements, read in 64 x 64 boxes with 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* m, const void* pool, const locks_cfg_t* c) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(c->head_dim),
+                              cuuint64_t(c->num_blocks) * c->n_kv_heads * c->page_size};
+  const cuuint64_t strides[1] = {cuuint64_t(c->head_dim) * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int decode_common(const locks_cfg_t* cfg, const void* q, const void* k_cache, const void* v_cache,
@@ -94,8 +123,13 @@ int decode_common(const locks_cfg_t* cfg, const void* q, const void* k_cache, co
   p.n_splits_max = L.n_splits_max;
   p.scale = float(1.0 / std::sqrt(double(cfg->head_dim)));
   p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(cfg->head_dim)));
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return LOCKS_ERR_INVALID_ARG;                     // tensor maps need 16-byte bases
+  CUtensorMap tk, tv;
+  if (!encode_pool_map(&tk, k_cache, cfg) || !encode_pool_map(&tv, v_cache, cfg))
+    return LOCKS_ERR_CUDA;
   const int U = cfg->batch * cfg->n_kv_heads;
-  return locks::launch_decode(p, group_of(cfg), L.n_splits_max, U,
+  return locks::launch_decode(p, tk, tv, group_of(cfg), L.n_splits_max, U,
                               static_cast<cudaStream_t>(stream));
 }
 

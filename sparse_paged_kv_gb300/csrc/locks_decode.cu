@@ -6,17 +6,22 @@
 //
 // CTA (split s, unit u = (sequence b, KV head h)) handles pages
 // [s*P, (s+1)*P) of the unit's page list.  Warp 4 is a producer: its lane 0
-// bulk-copies the valid token rows of each page's K and V (contiguous
-// [B][d] bf16 rows in the pool) into a STAGES-deep shared-memory ring,
+// loads each page's K and V (four 64-row x 64-column bf16 boxes through two
+// 2-D tensor maps, 128-byte swizzle) into a STAGES-deep shared-memory ring,
 // completing on a "full" mbarrier; consumer warps 0..3 release a slot on an
 // "empty" mbarrier.  Consumer warp w owns tokens [16w, 16w+16) of every page
-// and keeps, for each of the G query heads of the group, a running max m,
-// running sum l and an unnormalised output accumulator (dims [4l, 4l+4) in
-// lane l).  Scores: 8 lanes per token (16 dims each), 4 tokens per step,
-// reduced with a transposed 8-lane reduction.  At the end the four warp states
-// are merged, the split writes (m, l, acc) to the workspace, and the last split
-// of the unit (atomic ticket) merges all splits by their log-sum-exp and writes
-// the bf16 output and the natural-log lse.
+// and uses the tensor cores:
+//   S (16 x 16)  = Q_pad (16 x 128) . K_w^T       the G query heads are rows
+//                                                 0..G-1 of a zero-padded Q
+//   O (16 x 128) += P (16 x 16) . V_w (16 x 128)  P re-used from the S
+//                                                 accumulators as bf16
+// (mma.sync m16n8k16, bf16 inputs, fp32 accumulation; K fragments through
+// ldmatrix, V through ldmatrix.trans), with a per-head online softmax (running
+// max m, running sum l).  Tokens past the page's valid count are masked and
+// their V rows zeroed, so no value outside the sequence enters a product.
+// At the end the four warp states are merged, the split writes (m, l, acc)
+// to the workspace, and the last split of the unit (atomic ticket) merges all
+// splits by their log-sum-exp and writes the bf16 output and the lse.
 #include "locks_common.cuh"
 #include "locks_internal.h"
 
@@ -27,11 +32,9 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTokPerWarp = kPageSize / kConsumerWarps;    // 16
-constexpr int kRowBytes = kHeadDim * 2;                    // 256
-constexpr int kPageBytes = kPageSize * kRowBytes;          // 16 KiB
-constexpr int kSlotBytes = 2 * kPageBytes;                 // K then V
-
-constexpr int kMaxPagesPerSplit = 64;
+constexpr int kBoxBytes = 64 * 128;                        // 64 rows x 64 bf16
+constexpr int kSlotBytes = 4 * kBoxBytes;                  // K0 K1 V0 V1 (32 KiB)
+constexpr int kMaxPagesPerSplit = 256;
 
 // float max through the integer atomics (ordering of IEEE bit patterns)
 __device__ __forceinline__ void atomicMax_float(float* addr, float v) {
@@ -39,14 +42,53 @@ __device__ __forceinline__ void atomicMax_float(float* addr, float v) {
   else atomicMin(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
 }
 
-template <int G>
-__host__ __device__ constexpr int warp_buf_floats() {
-  return ((2 * G * kTokPerWarp + 3 * G) + 3) / 4 * 4;
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D += A . B for one m16n8k16 tile (bf16 in, fp32 accumulate)
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// shared-memory address of (row, 16-byte chunk) in a 64 x 128-byte box
+// written by a tensor load with 128-byte swizzle (box base 1024-byte aligned)
+__device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk) {
+  return box + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
 template <int G, int STAGES>
-__global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(kDecThreads)
+    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v) {
+  extern __shared__ __align__(1024) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
   const int u = blockIdx.y, sp = blockIdx.x;
   const int b = u / p.n_kv_heads, h = u % p.n_kv_heads;
@@ -70,14 +112,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
   const int cnt = max(0, min(n_list, i_lo + p.pages_per_split) - i_lo);
 
   // ---- shared memory ------------------------------------------------------
-  unsigned char* ring = smem;
+  unsigned char* ring = smem;                                       // STAGES x 32 KiB
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(STAGES) * kSlotBytes);
   uint64_t* empty = full + STAGES;
   int* slot_nv = reinterpret_cast<int*>(empty + STAGES);
-  float* wbuf_all = reinterpret_cast<float*>(slot_nv + ((STAGES + 3) / 4) * 4);
+  float* wstate = reinterpret_cast<float*>(slot_nv + 4);            // [4][2G]
+  __shared__ int s_blk[kMaxPagesPerSplit], s_nv[kMaxPagesPerSplit];
   __shared__ int s_is_last;
 
-  __shared__ int s_blk[kMaxPagesPerSplit], s_nv[kMaxPagesPerSplit];
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full + s, 1);
@@ -102,15 +144,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
   }
   __syncthreads();
 
-  float acc[G][4];
+  // per-lane accumulator of O rows g (= lane / 4) and g + 8, dims 8j + 2t, +1
+  float oacc[16][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
-  float* wb = wbuf_all + warp * warp_buf_floats<G>();
-  float* s_buf = wb;                              // [G][16] raw scores
-  float* p_buf = wb + G * kTokPerWarp;            // [16][G] probabilities
-  float* run_m = p_buf + G * kTokPerWarp;         // [G]
-  float* run_l = run_m + G;                       // [G]
-  float* alpha_buf = run_l + G;                   // [G]
+  for (int j = 0; j < 16; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+  const int g = lane >> 2, t4 = lane & 3;
+  float m_run = -INFINITY, l_run = 0.f;            // head g (lanes of a quad agree)
 
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
@@ -124,11 +163,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
         const int nv = s_nv[i], blk = s_blk[i];
         slot_nv[s] = nv;
         if (nv > 0) {
-          const size_t off = (size_t(blk) * p.n_kv_heads + h) * (B * kHeadDim);
-          const uint32_t bytes = uint32_t(nv) * kRowBytes;
-          mbar_arrive_expect_tx(full + s, 2 * bytes);
-          bulk_g2s(ring + size_t(s) * kSlotBytes, p.k_cache + off, bytes, full + s);
-          bulk_g2s(ring + size_t(s) * kSlotBytes + kPageBytes, p.v_cache + off, bytes, full + s);
+          const int row = (blk * p.n_kv_heads + h) * B;
+          unsigned char* slot = ring + size_t(s) * kSlotBytes;
+          mbar_arrive_expect_tx(full + s, kSlotBytes);
+          tma_load_2d(slot, &tmap_k, 0, row, full + s);
+          tma_load_2d(slot + kBoxBytes, &tmap_k, 64, row, full + s);
+          tma_load_2d(slot + 2 * kBoxBytes, &tmap_v, 0, row, full + s);
+          tma_load_2d(slot + 3 * kBoxBytes, &tmap_v, 64, row, full + s);
         } else {
           mbar_arrive(full + s);
         }
@@ -136,31 +177,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
     }
   } else {
     // ---------------- consumers ----------------
-    const int dsub = lane & 7, tsub = lane >> 3;
-    // query dims [8*dsub, 8*dsub+8) and [64+8*dsub, 64+8*dsub+8)
-    float qf[G][16];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
+    // Q fragments (rows = heads, zero beyond G): k-step ks covers dims [16ks, 16ks+16)
+    uint32_t qa0[8], qa2[8];
+    {
       const __nv_bfloat16* qg = p.q + (size_t(b) * (p.n_kv_heads * G) + h * G + g) * kHeadDim;
-      const uint4 a = *reinterpret_cast<const uint4*>(qg + 8 * dsub);
-      const uint4 c = *reinterpret_cast<const uint4*>(qg + 64 + 8 * dsub);
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        qf[g][2 * e] = bf16_lo(w[e]);
-        qf[g][2 * e + 1] = bf16_hi(w[e]);
+      for (int ks = 0; ks < 8; ++ks) {
+        qa0[ks] = g < G ? *reinterpret_cast<const uint32_t*>(qg + 16 * ks + 2 * t4) : 0u;
+        qa2[ks] = g < G ? *reinterpret_cast<const uint32_t*>(qg + 16 * ks + 8 + 2 * t4) : 0u;
       }
     }
-    if (lane < G) {
-      run_m[lane] = -INFINITY;
-      run_l[lane] = 0.f;
-    }
-    __syncwarp();
-
-    constexpr int LPH = 32 / G;                                 // softmax lanes per head
-    constexpr int TPL = LPH >= kTokPerWarp ? 1 : kTokPerWarp / LPH;
-    const int hg = lane / LPH, li = lane % LPH;
-    const int base = warp * kTokPerWarp;
+    const int n0 = warp * kTokPerWarp;
     int done = cnt;
     bool aborted = false;
     for (int i = 0; i < cnt; ++i) {
@@ -172,84 +199,74 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
         break;
       }
       const int nv = slot_nv[s];
-      if (nv > base) {
-        const unsigned char* Ks = ring + size_t(s) * kSlotBytes;
-        const unsigned char* Vs = Ks + kPageBytes;
-        // ---- scores of this warp's 16 tokens ----
-#pragma unroll
-        for (int it = 0; it < kTokPerWarp / 4; ++it) {
-          const int t = base + 4 * it + tsub;
-          float part[G];
-#pragma unroll
-          for (int g = 0; g < G; ++g) part[g] = 0.f;
-          if (t < nv) {
-            const uint4 a = *reinterpret_cast<const uint4*>(Ks + t * kRowBytes + 16 * dsub);
-            const uint4 c = *reinterpret_cast<const uint4*>(Ks + t * kRowBytes + 128 + 16 * dsub);
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float k0 = bf16_lo(w[e]), k1 = bf16_hi(w[e]);
-#pragma unroll
-              for (int g = 0; g < G; ++g) part[g] += qf[g][2 * e] * k0 + qf[g][2 * e + 1] * k1;
-            }
-          }
-          TransposeReduce<G, 4>::run(part, lane);
-          // lane holds head dsub / (8/G) (G <= 8) for token t
-          constexpr int SG = G < 8 ? G : 8;
-          if ((dsub & (8 / SG - 1)) == 0)
-            s_buf[(dsub / (8 / SG)) * kTokPerWarp + 4 * it + tsub] = t < nv ? part[0] : -INFINITY;
-        }
-        __syncwarp();
-        // ---- online softmax, head hg handled by lanes [hg*LPH, (hg+1)*LPH) ----
+      if (nv > n0) {
+        const uint32_t kbox = smem_u32(ring + size_t(s) * kSlotBytes);
+        const uint32_t vbox = kbox + 2 * kBoxBytes;
+        // ---- S = Q K^T over this warp's 16 tokens (two 8-token tiles) ----
+        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
-          float sv[TPL];
-          float mt = -INFINITY;
+          const int mi = lane >> 3, r = lane & 7;
+          const int tok = n0 + ((mi >> 1) << 3) + r;
 #pragma unroll
-          for (int m = 0; m < TPL; ++m) {
-            const int tl = li + LPH * m;
-            sv[m] = tl < kTokPerWarp ? s_buf[hg * kTokPerWarp + tl] : -INFINITY;
-            mt = fmaxf(mt, sv[m]);
+          for (int ks = 0; ks < 8; ++ks) {
+            uint32_t kb[4];
+            ldsm_x4(swz(kbox + (ks >> 2) * kBoxBytes, tok, 2 * (ks & 3) + (mi & 1)), kb);
+            mma16816(sacc[0], qa0[ks], 0u, qa2[ks], 0u, kb[0], kb[1]);
+            mma16816(sacc[1], qa0[ks], 0u, qa2[ks], 0u, kb[2], kb[3]);
           }
-          mt = group_max<LPH>(mt);
-          const float m_old = run_m[hg];
-          const float m_new = fmaxf(m_old, mt);
-          const float alpha = exp2f((m_old - m_new) * p.scale_log2);
-          float ls = 0.f;
+        }
+        // ---- online softmax for head g over tokens n0 + {2t, 2t+1, 8+2t, 9+2t} ----
+        const int tk0 = n0 + 2 * t4;
+        float sv[4] = {sacc[0][0], sacc[0][1], sacc[1][0], sacc[1][1]};
+        const int tks[4] = {tk0, tk0 + 1, tk0 + 8, tk0 + 9};
+        float mt = -INFINITY;
 #pragma unroll
-          for (int m = 0; m < TPL; ++m) {
-            const int tl = li + LPH * m;
-            const float pr = exp2f((sv[m] - m_new) * p.scale_log2);
-            if (tl < kTokPerWarp) p_buf[tl * G + hg] = pr;
-            ls += pr;
+        for (int e = 0; e < 4; ++e) {
+          sv[e] = tks[e] < nv ? sv[e] : -INFINITY;
+          mt = fmaxf(mt, sv[e]);
+        }
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+        const float m_new = fmaxf(m_run, mt);          // finite: the warp has a valid token
+        const float alpha = ex2_approx((m_run - m_new) * p.scale_log2);   // 0 when m_run = -inf
+        float pr[4], rs = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          pr[e] = (g < G) ? ex2_approx((sv[e] - m_new) * p.scale_log2) : 0.f;
+          rs += pr[e];
+        }
+        rs += __shfl_xor_sync(kFull, rs, 1);
+        rs += __shfl_xor_sync(kFull, rs, 2);
+        l_run = l_run * alpha + rs;
+        m_run = m_new;
+        if (__any_sync(kFull, alpha != 1.f)) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) { oacc[j][0] *= alpha; oacc[j][1] *= alpha; }
+        }
+        const uint32_t pa0 = pack_bf16(pr[0], pr[1]), pa2 = pack_bf16(pr[2], pr[3]);
+        // ---- tokens past the valid count: zero their V rows (never 0 x NaN) ----
+        if (nv < n0 + kTokPerWarp) {
+          for (int r = max(nv, n0); r < n0 + kTokPerWarp; ++r) {
+            unsigned char* row0 = ring + size_t(s) * kSlotBytes + 2 * kBoxBytes + r * 128;
+            if (lane < 8) *reinterpret_cast<uint4*>(row0 + lane * 16) = make_uint4(0, 0, 0, 0);
+            else if (lane < 16)
+              *reinterpret_cast<uint4*>(row0 + kBoxBytes + (lane - 8) * 16) = make_uint4(0, 0, 0, 0);
           }
-          ls = group_sum<LPH>(ls);
-          const float l_old = run_l[hg];
           __syncwarp();
-          if (li == 0) {
-            run_m[hg] = m_new;
-            run_l[hg] = l_old * alpha + ls;
-            alpha_buf[hg] = alpha;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        // ---- O += P V over dims 16j .. 16j+15 ----
+        {
+          const int mi = lane >> 3, r = lane & 7;
+          const int tok = n0 + ((mi & 1) << 3) + r;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t vb[4];
+            ldsm_x4_t(swz(vbox + (j >> 2) * kBoxBytes, tok, 2 * (j & 3) + (mi >> 1)), vb);
+            mma16816(oacc[2 * j], pa0, 0u, pa2, 0u, vb[0], vb[1]);
+            mma16816(oacc[2 * j + 1], pa0, 0u, pa2, 0u, vb[2], vb[3]);
           }
         }
-        __syncwarp();
-        // ---- acc = acc * alpha + P V over this warp's valid tokens ----
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float a = alpha_buf[g];
-          acc[g][0] *= a; acc[g][1] *= a; acc[g][2] *= a; acc[g][3] *= a;
-        }
-        const int ntok = min(kTokPerWarp, nv - base);
-        for (int tl = 0; tl < ntok; ++tl) {
-          const float4 v = bf16x4_to_f4(
-              *reinterpret_cast<const uint2*>(Vs + (base + tl) * kRowBytes + 8 * lane));
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float pr = p_buf[tl * G + g];
-            acc[g][0] += pr * v.x; acc[g][1] += pr * v.y;
-            acc[g][2] += pr * v.z; acc[g][3] += pr * v.w;
-          }
-        }
-        __syncwarp();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + s);
@@ -264,31 +281,37 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
   // ---- merge the four warp states into the split's partial ----------------
   float* mbuf = reinterpret_cast<float*>(ring);    // [4][G][128], the ring is idle now
   if (warp < kConsumerWarps) {
+    if (g < G) {
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      *reinterpret_cast<float4*>(mbuf + (warp * G + g) * kHeadDim + 4 * lane) =
-          make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+      for (int j = 0; j < 16; ++j)
+        *reinterpret_cast<float2*>(mbuf + (warp * G + g) * kHeadDim + 8 * j + 2 * t4) =
+            make_float2(oacc[j][0], oacc[j][1]);
+      if (t4 == 0) {
+        wstate[warp * 2 * G + g] = m_run;
+        wstate[warp * 2 * G + G + g] = l_run;
+      }
+    }
   }
   __syncthreads();
   const size_t part_stride = kPartStride;   // [m, l, pad, pad, acc[d]]: acc 16-byte aligned
   float* part = p.ws_part + (size_t(u) * p.n_splits_max + sp) * G * part_stride;
   for (int t = tid; t < G * 32; t += kDecThreads) {
-    const int g = t >> 5, l4 = t & 31;
+    const int gg = t >> 5, l4 = t & 31;
     float M = -INFINITY;
-    for (int w = 0; w < kConsumerWarps; ++w)
-      M = fmaxf(M, wbuf_all[w * warp_buf_floats<G>() + 2 * G * kTokPerWarp + g]);
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wstate[w * 2 * G + gg]);
     float L = 0.f;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float* wbw = wbuf_all + w * warp_buf_floats<G>() + 2 * G * kTokPerWarp;
-        const float f = exp2f((wbw[g] - M) * p.scale_log2);
-        L += wbw[G + g] * f;
-        const float4 a = *reinterpret_cast<const float4*>(mbuf + (w * G + g) * kHeadDim + 4 * l4);
+        const float mw = wstate[w * 2 * G + gg];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f((mw - M) * p.scale_log2);
+        L += wstate[w * 2 * G + G + gg] * f;
+        const float4 a = *reinterpret_cast<const float4*>(mbuf + (w * G + gg) * kHeadDim + 4 * l4);
         A.x += a.x * f; A.y += a.y * f; A.z += a.z * f; A.w += a.w * f;
       }
     }
-    float* pg = part + g * part_stride;
+    float* pg = part + gg * part_stride;
     if (l4 == 0) { pg[0] = M; pg[1] = L; }
     *reinterpret_cast<float4*>(pg + 4 + 4 * l4) = A;
   }
@@ -305,21 +328,21 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
   if (tid < G) s_mmax[tid] = -INFINITY;
   __syncthreads();
   for (int t = tid; t < nsplits * G; t += kDecThreads) {
-    const int s2 = t / G, g = t % G;
-    const float m2 = __ldcg(p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + g) * part_stride);
-    if (m2 != -INFINITY) atomicMax_float(s_mmax + g, m2);
+    const int s2 = t / G, gg = t % G;
+    const float m2 = __ldcg(p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + gg) * part_stride);
+    if (m2 != -INFINITY) atomicMax_float(s_mmax + gg, m2);
   }
   __syncthreads();
   // ... then the rescaled sums, whose loads no longer depend on each other
   for (int t = tid; t < G * 32; t += kDecThreads) {
-    const int g = t >> 5, l4 = t & 31;
-    const float M = s_mmax[g];
+    const int gg = t >> 5, l4 = t & 31;
+    const float M = s_mmax[gg];
     float L = 0.f;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
 #pragma unroll 8
       for (int s2 = 0; s2 < nsplits; ++s2) {
-        const float* pg = p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + g) * part_stride;
+        const float* pg = p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + gg) * part_stride;
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg));
         const float4 a2 = __ldcg(reinterpret_cast<const float4*>(pg + 4 + 4 * l4));
         const float f = ml.x == -INFINITY ? 0.f : exp2f((ml.x - M) * p.scale_log2);
@@ -328,7 +351,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat16* o = p.out + (size_t(b) * (p.n_kv_heads * G) + h * G + g) * kHeadDim + 4 * l4;
+    __nv_bfloat16* o = p.out + (size_t(b) * (p.n_kv_heads * G) + h * G + gg) * kHeadDim + 4 * l4;
     const __nv_bfloat162 o01 = __floats2bfloat162_rn(A.x * inv, A.y * inv);
     const __nv_bfloat162 o23 = __floats2bfloat162_rn(A.z * inv, A.w * inv);
     uint2 ow;
@@ -336,18 +359,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeParams 
     ow.y = *reinterpret_cast<const uint32_t*>(&o23);
     *reinterpret_cast<uint2*>(o) = ow;
     if (l4 == 0 && p.out_lse)
-      p.out_lse[size_t(b) * (p.n_kv_heads * G) + h * G + g] =
+      p.out_lse[size_t(b) * (p.n_kv_heads * G) + h * G + gg] =
           L > 0.f ? M * p.scale + logf(L) : -INFINITY;
   }
   if (tid == 0) p.ws_ticket[u] = 0;
 }
 
 template <int G>
-int launch_g(const DecodeParams& p, int gx, int gy, cudaStream_t stream) {
+int launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int gx, int gy,
+             cudaStream_t stream) {
   constexpr int STAGES = 3;
   const size_t smem = size_t(STAGES) * kSlotBytes + 2 * STAGES * sizeof(uint64_t) +
-                      ((STAGES + 3) / 4) * 4 * sizeof(int) +
-                      kConsumerWarps * warp_buf_floats<G>() * sizeof(float);
+                      4 * sizeof(int) + kConsumerWarps * 2 * G * sizeof(float);
   auto kern = decode_kernel<G, STAGES>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
@@ -362,17 +385,29 @@ int launch_g(const DecodeParams& p, int gx, int gy, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kern, p) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
+  return cudaLaunchKernelEx(&lc, kern, p, tk, tv) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_decode(const DecodeParams& p, int G, int gx, int gy, cudaStream_t stream) {
+int decode_pages_per_split(long units, int n_pages) {
+  // about one wave of two CTAs per SM on 152 SMs for small page lists, two
+  // for large ones; at most kMaxPagesPerSplit pages per CTA
+  const long total = units * (n_pages > 0 ? n_pages : 1);
+  const long waves = total > 16384 ? 2 : 1;
+  long pps = (total + waves * 2 * 152 - 1) / (waves * 2 * 152);
+  if (pps < 1) pps = 1;
+  if (pps > kMaxPagesPerSplit) pps = kMaxPagesPerSplit;
+  return int(pps);
+}
+
+int launch_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int G,
+                  int gx, int gy, cudaStream_t stream) {
   switch (G) {
-    case 1: return launch_g<1>(p, gx, gy, stream);
-    case 2: return launch_g<2>(p, gx, gy, stream);
-    case 4: return launch_g<4>(p, gx, gy, stream);
-    case 8: return launch_g<8>(p, gx, gy, stream);
+    case 1: return launch_g<1>(p, tk, tv, gx, gy, stream);
+    case 2: return launch_g<2>(p, tk, tv, gx, gy, stream);
+    case 4: return launch_g<4>(p, tk, tv, gx, gy, stream);
+    case 8: return launch_g<8>(p, tk, tv, gx, gy, stream);
     default: return LOCKS_ERR_UNSUPPORTED;
   }
 }

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -79,7 +80,9 @@ struct BuildParams {
 SelectGeom select_geometry(int units, int max_pages, int G, int k);
 int launch_select(const SelectParams& p, int G, int RP, int dtype, int n_score_ctas,
                   int n_slices, cudaStream_t stream);
-int launch_decode(const DecodeParams& p, int G, int grid_x, int grid_y, cudaStream_t stream);
+int decode_pages_per_split(long units, int n_pages);
+int launch_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int G,
+                  int grid_x, int grid_y, cudaStream_t stream);
 int launch_build(const BuildParams& p, int RP, int dtype, cudaStream_t stream);
 
 }  // namespace locks
