@@ -137,6 +137,7 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
 // packed fp32 FMA (two lanes of fp32 per instruction on sm_100+)

@@ -19,9 +19,19 @@
 // ldmatrix, V through ldmatrix.trans), with a per-head online softmax (running
 // max m, running sum l).  Tokens past the page's valid count are masked and
 // their V rows zeroed, so no value outside the sequence enters a product.
-// At the end the four warp states are merged, the split writes (m, l, acc)
-// to the workspace, and the last split of the unit (atomic ticket) merges all
-// splits by their log-sum-exp and writes the bf16 output and the lse.
+// At the end the four warp states are merged into the split's (m, l, acc).
+// The splits of a unit are then combined by their log-sum-exp in one of two
+// ways:
+//   * clustered (page lists of equal length, i.e. the selected pages): the C
+//     splits of a unit form one thread-block cluster; each keeps its partial
+//     in its own shared memory, and after a cluster barrier CTA r reads all C
+//     partials through distributed shared memory and writes its share of the
+//     bf16 output rows;
+//   * ticketed (every page, lists of unequal length): each split writes its
+//     partial to the workspace and the last split of the unit (atomic ticket)
+//     merges them.
+#include <algorithm>
+
 #include "locks_common.cuh"
 #include "locks_internal.h"
 
@@ -35,6 +45,7 @@ constexpr int kTokPerWarp = kPageSize / kConsumerWarps;    // 16
 constexpr int kBoxBytes = 64 * 128;                        // 64 rows x 64 bf16
 constexpr int kSlotBytes = 4 * kBoxBytes;                  // K0 K1 V0 V1 (32 KiB)
 constexpr int kMaxPagesPerSplit = 256;
+constexpr int kMaxClusterSplits = 16;                      // cluster size limit (non-portable above 8)
 
 // float max through the integer atomics (ordering of IEEE bit patterns)
 __device__ __forceinline__ void atomicMax_float(float* addr, float v) {
@@ -78,13 +89,57 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// distributed shared memory: the address of the same variable in CTA `rank`
+// of the cluster, and loads from it
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+// every thread of every CTA of the cluster; shared-memory writes before it are
+// visible to the cluster's loads after it
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release;\n"
+      "barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void store_out_row(const DecodeParams& p, int b, int h, int G, int gg,
+                                              int l4, float4 A, float L, float M) {
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* o = p.out + (size_t(b) * (p.n_kv_heads * G) + h * G + gg) * kHeadDim + 4 * l4;
+  const __nv_bfloat162 o01 = __floats2bfloat162_rn(A.x * inv, A.y * inv);
+  const __nv_bfloat162 o23 = __floats2bfloat162_rn(A.z * inv, A.w * inv);
+  uint2 ow;
+  ow.x = *reinterpret_cast<const uint32_t*>(&o01);
+  ow.y = *reinterpret_cast<const uint32_t*>(&o23);
+  *reinterpret_cast<uint2*>(o) = ow;
+  if (l4 == 0 && p.out_lse)
+    p.out_lse[size_t(b) * (p.n_kv_heads * G) + h * G + gg] =
+        L > 0.f ? M * p.scale + logf(L) : -INFINITY;
+}
+
 // shared-memory address of (row, 16-byte chunk) in a 64 x 128-byte box
 // written by a tensor load with 128-byte swizzle (box base 1024-byte aligned)
 __device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk) {
   return box + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <int G, int STAGES>
+template <int G, int STAGES, bool CLUSTERED>
 __global__ void __launch_bounds__(kDecThreads)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v) {
@@ -93,23 +148,6 @@ __global__ void __launch_bounds__(kDecThreads)
   const int u = blockIdx.y, sp = blockIdx.x;
   const int b = u / p.n_kv_heads, h = u % p.n_kv_heads;
   constexpr int B = kPageSize;
-
-  // launched as a programmatic dependent of the previous kernel on the stream:
-  // wait for it to finish before reading anything it may have written
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  int seq_len = p.seq_lens[b];
-  if (seq_len > p.max_pages * B) {
-    if (sp == 0 && tid == 0) flag_status(p.status, LOCKS_DEV_BAD_SEQ_LEN);
-    seq_len = p.max_pages * B;
-  }
-  if (seq_len < 0) seq_len = 0;
-  const int n = (seq_len + B - 1) / B;
-  const int n_list = p.selected ? p.k : n;
-  const int nsplits = max(1, (n_list + p.pages_per_split - 1) / p.pages_per_split);
-  if (sp >= nsplits) return;
-  const int i_lo = sp * p.pages_per_split;
-  const int cnt = max(0, min(n_list, i_lo + p.pages_per_split) - i_lo);
 
   // ---- shared memory ------------------------------------------------------
   unsigned char* ring = smem;                                       // STAGES x 32 KiB
@@ -120,6 +158,8 @@ __global__ void __launch_bounds__(kDecThreads)
   __shared__ int s_blk[kMaxPagesPerSplit], s_nv[kMaxPagesPerSplit];
   __shared__ int s_is_last;
 
+  // set-up that touches no memory a previous kernel may write runs before
+  // the dependency wait
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full + s, 1);
@@ -127,10 +167,44 @@ __global__ void __launch_bounds__(kDecThreads)
     }
     mbar_fence_init();
   }
+  if (warp == kConsumerWarps && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_k) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_v) : "memory");
+  }
+
+  // launched as a programmatic dependent of the previous kernel on the stream:
+  // wait for it to finish before reading anything it may have written
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // the sequence length and (for a selected list, whose length is the same for
+  // every unit) this thread's first page id are loaded together
+  int seq_len = p.seq_lens[b];
+  int j_first = -1;
+  if (p.selected) {
+    const int lo = sp * p.pages_per_split;
+    if (tid < min(p.k, lo + p.pages_per_split) - lo)
+      j_first = p.selected[size_t(u) * p.k + lo + tid];
+  }
+  if (seq_len > p.max_pages * B) {
+    if (sp == 0 && tid == 0) flag_status(p.status, LOCKS_DEV_BAD_SEQ_LEN);
+    seq_len = p.max_pages * B;
+  }
+  if (seq_len < 0) seq_len = 0;
+  const int n = (seq_len + B - 1) / B;
+  const int n_list = p.selected ? p.k : n;
+  const int nsplits = CLUSTERED ? int(gridDim.x)
+                                : max(1, (n_list + p.pages_per_split - 1) / p.pages_per_split);
+  // (a clustered launch has exactly the unit's splits: no CTA leaves early, so
+  // every thread reaches the cluster barriers)
+  if (!CLUSTERED && sp >= nsplits) return;
+  const int i_lo = sp * p.pages_per_split;
+  const int cnt = max(0, min(n_list, i_lo + p.pages_per_split) - i_lo);
+
   // page ids of this split: block and valid tokens, checked once
   const int32_t* bt = p.block_table + size_t(b) * p.max_pages;
   for (int t = tid; t < cnt; t += kDecThreads) {
-    const int j = p.selected ? p.selected[size_t(u) * p.k + i_lo + t] : i_lo + t;
+    const int j = p.selected ? (t == tid ? j_first : p.selected[size_t(u) * p.k + i_lo + t])
+                             : i_lo + t;
     int nv = 0, blk = -1;
     if (j >= 0 && j < n) {
       blk = bt[j];
@@ -294,7 +368,11 @@ __global__ void __launch_bounds__(kDecThreads)
   }
   __syncthreads();
   const size_t part_stride = kPartStride;   // [m, l, pad, pad, acc[d]]: acc 16-byte aligned
-  float* part = p.ws_part + (size_t(u) * p.n_splits_max + sp) * G * part_stride;
+  // the split's partial: in this CTA's shared memory (clustered), past the
+  // warp accumulators in the idle ring, or in the workspace (ticketed)
+  float* part = CLUSTERED
+                    ? reinterpret_cast<float*>(ring + kConsumerWarps * G * kHeadDim * sizeof(float))
+                    : p.ws_part + (size_t(u) * p.n_splits_max + sp) * G * part_stride;
   for (int t = tid; t < G * 32; t += kDecThreads) {
     const int gg = t >> 5, l4 = t & 31;
     float M = -INFINITY;
@@ -315,6 +393,52 @@ __global__ void __launch_bounds__(kDecThreads)
     if (l4 == 0) { pg[0] = M; pg[1] = L; }
     *reinterpret_cast<float4*>(pg + 4 + 4 * l4) = A;
   }
+
+  if constexpr (CLUSTERED) {
+    // ---- merge the unit's splits through distributed shared memory ----------
+    // CTA sp writes output entries [sp * per, (sp + 1) * per) of the unit's
+    // G x 32 (head, 4-dim chunk) entries
+    __syncthreads();
+    cluster_sync_all();
+    const int C = nsplits;
+    const int per = (G * 32 + C - 1) / C;
+    const int t_end = min(G * 32, (sp + 1) * per);
+    for (int t = sp * per + tid; t < t_end; t += kDecThreads) {
+      const int gg = t >> 5, l4 = t & 31;
+      const uint32_t a_ml = smem_u32(part + gg * part_stride);
+      const uint32_t a_acc = a_ml + (4 + 4 * l4) * sizeof(float);
+      float2 ml[kMaxClusterSplits];
+      float4 ac[kMaxClusterSplits];
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSplits; ++r) {
+        if (r < C) {
+          ml[r] = ld_dsmem_f2(dsmem_addr(a_ml, r));
+          ac[r] = ld_dsmem_f4(dsmem_addr(a_acc, r));
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSplits; ++r)
+        if (r < C) M = fmaxf(M, ml[r].x);
+      float L = 0.f;
+      float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < kMaxClusterSplits; ++r) {
+          if (r < C && ml[r].x != -INFINITY) {
+            const float f = exp2f((ml[r].x - M) * p.scale_log2);
+            L += ml[r].y * f;
+            A.x += ac[r].x * f; A.y += ac[r].y * f; A.z += ac[r].z * f; A.w += ac[r].w * f;
+          }
+        }
+      }
+      store_out_row(p, b, h, G, gg, l4, A, L, M);
+    }
+    // no CTA leaves while another may still read its shared memory
+    cluster_sync_all();
+    return;
+  }
+
   __threadfence();
   __syncthreads();
   if (tid == 0) s_is_last = (atomicAdd(p.ws_ticket + u, 1) == nsplits - 1);
@@ -350,28 +474,58 @@ __global__ void __launch_bounds__(kDecThreads)
         A.x += a2.x * f; A.y += a2.y * f; A.z += a2.z * f; A.w += a2.w * f;
       }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat16* o = p.out + (size_t(b) * (p.n_kv_heads * G) + h * G + gg) * kHeadDim + 4 * l4;
-    const __nv_bfloat162 o01 = __floats2bfloat162_rn(A.x * inv, A.y * inv);
-    const __nv_bfloat162 o23 = __floats2bfloat162_rn(A.z * inv, A.w * inv);
-    uint2 ow;
-    ow.x = *reinterpret_cast<const uint32_t*>(&o01);
-    ow.y = *reinterpret_cast<const uint32_t*>(&o23);
-    *reinterpret_cast<uint2*>(o) = ow;
-    if (l4 == 0 && p.out_lse)
-      p.out_lse[size_t(b) * (p.n_kv_heads * G) + h * G + gg] =
-          L > 0.f ? M * p.scale + logf(L) : -INFINITY;
+    store_out_row(p, b, h, G, gg, l4, A, L, M);
   }
   if (tid == 0) p.ws_ticket[u] = 0;
 }
 
 template <int G>
-int launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int gx, int gy,
-             cudaStream_t stream) {
+constexpr size_t decode_smem_bytes(int stages) {
+  return size_t(stages) * kSlotBytes + 2 * stages * sizeof(uint64_t) + 4 * sizeof(int) +
+         kConsumerWarps * 2 * G * sizeof(float);
+}
+
+// Whether clusters of C decode CTAs can be resident on this device (queried
+// once per group size and cluster size).
+template <int G>
+bool cluster_fits(int C) {
+  static int known[kMaxClusterSplits + 1] = {};   // 0 unknown, 1 yes, -1 no
+  if (C < 1 || C > kMaxClusterSplits) return false;
+  int k = __atomic_load_n(&known[C], __ATOMIC_ACQUIRE);
+  if (k != 0) return k > 0;
   constexpr int STAGES = 3;
-  const size_t smem = size_t(STAGES) * kSlotBytes + 2 * STAGES * sizeof(uint64_t) +
-                      4 * sizeof(int) + kConsumerWarps * 2 * G * sizeof(float);
-  auto kern = decode_kernel<G, STAGES>;
+  auto kern = decode_kernel<G, STAGES, true>;
+  const size_t smem = decode_smem_bytes<G>(STAGES);
+  bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) ==
+                cudaSuccess &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                cudaSuccess;
+  if (ok) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(C, 1);
+    lc.blockDim = dim3(kDecThreads);
+    lc.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int n_clusters = 0;
+    ok = cudaOccupancyMaxActiveClusters(&n_clusters, kern, &lc) == cudaSuccess && n_clusters > 0;
+  }
+  if (!ok) cudaGetLastError();   // a refused query leaves no error behind
+  __atomic_store_n(&known[C], ok ? 1 : -1, __ATOMIC_RELEASE);
+  return ok;
+}
+
+template <int G>
+int launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int gx, int gy,
+             bool clustered, cudaStream_t stream) {
+  constexpr int STAGES = 3;
+  const size_t smem = decode_smem_bytes<G>(STAGES);
+  auto kern = clustered ? decode_kernel<G, STAGES, true> : decode_kernel<G, STAGES, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return LOCKS_ERR_CUDA;
@@ -380,23 +534,44 @@ int launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv
   lc.blockDim = dim3(kDecThreads);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = gx;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = clustered ? 2 : 1;
   return cudaLaunchKernelEx(&lc, kern, p, tk, tv) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
+}
+
+template <int G>
+int launch_list(DecodeParams p, const CUtensorMap& tk, const CUtensorMap& tv, int gx, int gy,
+                cudaStream_t stream) {
+  if (p.selected && p.k > 0) {
+    // equal-length lists: one cluster of at most kMaxClusterSplits splits per unit
+    const int pps = std::max(p.pages_per_split, (p.k + kMaxClusterSplits - 1) / kMaxClusterSplits);
+    const int C = (p.k + pps - 1) / pps;
+    if (cluster_fits<G>(C)) {
+      p.pages_per_split = pps;
+      return launch_g<G>(p, tk, tv, C, gy, true, stream);
+    }
+  }
+  return launch_g<G>(p, tk, tv, gx, gy, false, stream);
 }
 
 }  // namespace
 
 int decode_pages_per_split(long units, int n_pages) {
-  // about one wave of two CTAs per SM on 152 SMs for small page lists, two
-  // for large ones; at most kMaxPagesPerSplit pages per CTA
-  const long total = units * (n_pages > 0 ? n_pages : 1);
-  const long waves = total > 16384 ? 2 : 1;
-  long pps = (total + waves * 2 * 152 - 1) / (waves * 2 * 152);
-  if (pps < 1) pps = 1;
+  // a whole number of splits per unit such that all splits fit one wave of two
+  // CTAs per SM on 152 SMs (two waves for long page lists); at most
+  // kMaxPagesPerSplit pages per CTA
+  const long np = n_pages > 0 ? n_pages : 1;
+  const long waves = units * np > 16384 ? 2 : 1;
+  long splits = (waves * 2 * 152) / (units > 0 ? units : 1);
+  if (splits < 1) splits = 1;
+  long pps = (np + splits - 1) / splits;
   if (pps > kMaxPagesPerSplit) pps = kMaxPagesPerSplit;
   return int(pps);
 }
@@ -404,10 +579,10 @@ int decode_pages_per_split(long units, int n_pages) {
 int launch_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int G,
                   int gx, int gy, cudaStream_t stream) {
   switch (G) {
-    case 1: return launch_g<1>(p, tk, tv, gx, gy, stream);
-    case 2: return launch_g<2>(p, tk, tv, gx, gy, stream);
-    case 4: return launch_g<4>(p, tk, tv, gx, gy, stream);
-    case 8: return launch_g<8>(p, tk, tv, gx, gy, stream);
+    case 1: return launch_list<1>(p, tk, tv, gx, gy, stream);
+    case 2: return launch_list<2>(p, tk, tv, gx, gy, stream);
+    case 4: return launch_list<4>(p, tk, tv, gx, gy, stream);
+    case 8: return launch_list<8>(p, tk, tv, gx, gy, stream);
     default: return LOCKS_ERR_UNSUPPORTED;
   }
 }

@@ -393,6 +393,43 @@ __device__ __forceinline__ unsigned long long warp_top32_of_256(unsigned long lo
   return warp_merge_top32(v[0], v[4], lane);
 }
 
+// The warp's top 32 of its 256 keys, first discarding every key below the
+// smallest of the 32 lane maxima (at least 32 keys reach it, so the top 32 all
+// do); the survivors -- usually a few dozen -- are compacted through `stage`
+// (64 entries of shared memory) and sorted as two 32-lists.  More than 64
+// survivors fall back to sorting all 256.
+__device__ __forceinline__ unsigned long long warp_top32_filtered(unsigned long long (&v)[8],
+                                                                 unsigned long long* stage,
+                                                                 int lane) {
+  unsigned long long mx = v[0];
+#pragma unroll
+  for (int e = 1; e < 8; ++e) mx = v[e] > mx ? v[e] : mx;
+  unsigned long long thr = mx;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const unsigned long long x = shfl_xor64(thr, o);
+    thr = x < thr ? x : thr;
+  }
+  int mine = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mine += v[e] >= thr;
+  const int before = warp_incl_scan(mine, lane) - mine;
+  const int total = __shfl_sync(kFull, before + mine, 31);
+  if (total > 64) return warp_top32_of_256(v, lane);
+  stage[lane] = 0ull;
+  stage[32 + lane] = 0ull;
+  __syncwarp();
+  int at = before;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (v[e] >= thr) stage[at++] = v[e];
+  __syncwarp();
+  const unsigned long long a = warp_sort_desc(stage[lane], lane);
+  const unsigned long long b = warp_sort_desc(stage[32 + lane], lane);
+  __syncwarp();
+  return warp_merge_top32(a, b, lane);
+}
+
 // Writes the first K (<= 32) keys of a descending list as pages in increasing
 // page order to out[0..K).
 __device__ __forceinline__ void warp_emit_pages_ascending(unsigned long long top, int K,
@@ -516,6 +553,18 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   __shared__ float s_logz[16];
   __shared__ int s_cnt[kFinWarps];
   __shared__ int s_is_last;
+  const float* ws_s = p.ws_scores + size_t(u) * p.max_pages * G;
+  const int c_lo = sl * p.slice, c_n = min(n_cand, c_lo + p.slice) - c_lo;
+  // the register path's score loads go out first: they do not depend on log Z
+  float sv_early[8][G];
+  const bool early = n > k && K > 0 && K <= 32;
+  if (early) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int i = warp * 256 + 32 * e + lane;
+      if (i < c_n) ld_scores<G>(ws_s + size_t(1 + c_lo + i) * G, sv_early[e]);
+    }
+  }
   // shared memory: keys[cap] pages[cap] | warp winners wk/wp [8][K] | list lk/lp [8K] | hist [8][256]
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
   int* pages = reinterpret_cast<int*>(keys + p.fin_cap);
@@ -525,7 +574,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   int* lp = reinterpret_cast<int*>(lk + kFinWarps * K);
   unsigned* hist = reinterpret_cast<unsigned*>(lp + kFinWarps * K) + warp * 256;
 
-  // ---- log Z_g from the unit's partials -----------------------------------
+  // ---- log Z_g from the unit's partials: block max, then the rescaled sum ----
   {
     const int i_first = int((long(u) * p.mc) / p.per_cta);
     const int i_last = int((long(u + 1) * p.mc - 1) / p.per_cta);
@@ -542,38 +591,49 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
+      float mx = m[g];
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float m2 = __shfl_xor_sync(kFull, m[g], o), s2 = __shfl_xor_sync(kFull, s[g], o);
-        lse_merge(m[g], s[g], m2, s2);
-      }
-      if (lane == 0) { s_red[warp][g][0] = m[g]; s_red[warp][g][1] = s[g]; }
+      for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      if (lane == 0) s_red[warp][g][0] = mx;
+    }
+    __syncthreads();
+    float M[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      M[g] = s_red[0][g][0];
+      for (int w = 1; w < kFinWarps; ++w) M[g] = fmaxf(M[g], s_red[w][g][0]);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float x = (m[g] == -INFINITY) ? 0.f : s[g] * ex2_approx((m[g] - M[g]) * kLog2e);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+      if (lane == 0) s_red[warp][g][1] = x;
     }
     __syncthreads();
     if (tid < G) {
-      float mm = -INFINITY, ss = 0.f;
-      for (int w = 0; w < kFinWarps; ++w) lse_merge(mm, ss, s_red[w][tid][0], s_red[w][tid][1]);
-      s_logz[tid] = (ss > 0.f) ? mm + logf(ss) : -INFINITY;
+      float ss = 0.f, mt = -INFINITY;
+      for (int w = 0; w < kFinWarps; ++w) {
+        ss += s_red[w][tid][1];
+        mt = fmaxf(mt, s_red[w][tid][0]);
+      }
+      s_logz[tid] = (ss > 0.f && mt != -INFINITY) ? mt + kLn2 * lg2_approx(ss) : -INFINITY;
     }
     __syncthreads();
   }
 
   // ---- averaged shares of this slice's candidates ---------------------------
   // warp w owns entries [256w, 256w + 256) of the slice, lane l every 32nd
-  const int c_lo = sl * p.slice, c_n = min(n_cand, c_lo + p.slice) - c_lo;
   const bool select = n > k && K > 0;
-  const float* ws_s = p.ws_scores + size_t(u) * p.max_pages * G;
-  if (select && K <= 32) {
+  if (early) {
     // ---- register path: sorting networks, no shared-memory passes -------------
     __shared__ unsigned long long s_top[kFinWarps][32];
+    __shared__ unsigned long long s_stage[kFinWarps][64];
     unsigned long long v[8];
     {
-      float sv[8][G];
+      float lz2[G];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int i = warp * 256 + 32 * e + lane;
-        if (i < c_n) ld_scores<G>(ws_s + size_t(1 + c_lo + i) * G, sv[e]);
-      }
+      for (int g = 0; g < G; ++g) lz2[g] = s_logz[g] * kLog2e;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int i = warp * 256 + 32 * e + lane;
@@ -581,14 +641,15 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
         if (i < c_n) {
           float mb = 0.f;
 #pragma unroll
-          for (int g = 0; g < G; ++g) mb += expf(sv[e][g] - s_logz[g]);
+          for (int g = 0; g < G; ++g) mb += ex2_approx(fmaf(sv_early[e][g], kLog2e, -lz2[g]));
           mb *= 1.f / G;
           v[e] = cand_key(__float_as_uint(mb), uint32_t(1 + c_lo + i));
           if (p.page_share) p.page_share[size_t(u) * p.max_pages + 1 + c_lo + i] = mb;
         }
       }
     }
-    s_top[warp][lane] = warp_top32_of_256(v, lane);
+    // warps whose 256 entries lie past the slice's candidates hold nothing
+    s_top[warp][lane] = warp * 256 < c_n ? warp_top32_filtered(v, s_stage[warp], lane) : 0ull;
     __syncthreads();
     if (warp == 0) {
       unsigned long long t[kFinWarps];
