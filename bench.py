@@ -395,6 +395,23 @@ def run_gpu(args):
     mean_step = sum(step_ms) / K
     mean_step_max = reduce_max(mean_step, dist, "cuda")
 
+    # ---- the same step replayed from a CUDA graph ----
+    graph_ms, graph_err = None, None
+    try:
+        graph = layer.capture_step()
+
+        def gstep(ev):
+            if ev:
+                ev[0].record(stream)
+            graph.replay()
+            if ev:
+                ev[1].record(stream)
+
+        gevs, _ = timed(gstep, max(1, min(K, 500)), min(Wm, 10), marks=2)
+        graph_ms = [e[0].elapsed_time(e[1]) for e in gevs]
+    except RuntimeError as exc:          # reported in the JSON line, never hidden
+        graph_err = str(exc).splitlines()[0][:200]
+
     # ---- the two calls on their own (events between them), for the roofline ----
     K2 = max(1, min(K, 200))
 
@@ -486,7 +503,10 @@ def run_gpu(args):
         "step_us": {"mean": mean_step * 1e3, "median": statistics.median(step_ms) * 1e3,
                     "p10": sorted(step_ms)[K // 10] * 1e3, "p90": sorted(step_ms)[(9 * K) // 10] * 1e3,
                     "select_alone_mean": sel_mean * 1e3,
-                    "sparse_decode_alone_mean": sum(dec_ms) / len(dec_ms) * 1e3},
+                    "sparse_decode_alone_mean": sum(dec_ms) / len(dec_ms) * 1e3,
+                    "graph_replay_mean": (sum(graph_ms) / len(graph_ms) * 1e3) if graph_ms else None,
+                    "graph_replay_median": statistics.median(graph_ms) * 1e3 if graph_ms else None},
+        "graph_error": graph_err,
         "step_gbs": step_gbs,
         "step_frac": step_gbs / peak,
         "roofline": {"bound": "hbm", "kernel": "locks_select (score_kernel + finalize_kernel)",

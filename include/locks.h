@@ -100,6 +100,9 @@ typedef struct locks_cfg {
  */
 size_t locks_summary_record_bytes(const locks_cfg_t* cfg);
 
+/* Same value as locks_summary_record_bytes (the shorter name). */
+size_t locks_summary_bytes(const locks_cfg_t* cfg);
+
 /* Bytes of workspace locks_select needs for this cfg and token budget. */
 size_t locks_select_workspace_bytes(const locks_cfg_t* cfg, int32_t budget_tokens);
 

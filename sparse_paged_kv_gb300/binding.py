@@ -91,6 +91,7 @@ _lib = None
 _P = ctypes.c_void_p
 _SIGS = {
     "locks_summary_record_bytes": (ctypes.c_size_t, [ctypes.POINTER(locks_cfg_t)]),
+    "locks_summary_bytes": (ctypes.c_size_t, [ctypes.POINTER(locks_cfg_t)]),
     "locks_select_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(locks_cfg_t), ctypes.c_int32]),
     "locks_decode_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(locks_cfg_t), ctypes.c_int32]),
     "locks_build_summaries": (ctypes.c_int, [ctypes.POINTER(locks_cfg_t), _P, _P, ctypes.c_int32,

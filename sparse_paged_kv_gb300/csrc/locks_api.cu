@@ -143,6 +143,8 @@ size_t locks_summary_record_bytes(const locks_cfg_t* cfg) {
   return size_t(locks::rec_elems(rp, cfg->page_size)) * elem_bytes(cfg);
 }
 
+size_t locks_summary_bytes(const locks_cfg_t* cfg) { return locks_summary_record_bytes(cfg); }
+
 size_t locks_select_workspace_bytes(const locks_cfg_t* cfg, int32_t budget_tokens) {
   if (check_cfg(cfg) != LOCKS_OK) return 0;
   const int k = page_budget(budget_tokens, cfg->page_size);

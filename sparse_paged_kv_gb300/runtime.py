@@ -109,6 +109,24 @@ class LocksLayer:
         self.select(stream=stream)
         self.sparse_decode(stream=stream)
 
+    def capture_step(self):
+        """A CUDA graph of one sparse decode step (selection, then attention)
+        over this layer's buffers.  replay() runs it on the current stream and
+        reads q, seq_lens and block_table as they are at replay time.  The
+        step runs once outside the capture first, so one-time launch set-up
+        (kernel attributes, the cluster-size query) never happens inside it."""
+        torch = self.torch
+        cur = torch.cuda.current_stream(self.device)
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            self.step()
+        cur.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.step()
+        return graph
+
     # ---- diagnostics ------------------------------------------------------------
     def host_records(self, blocks, h: int):
         """(mu, V, C) of the given physical blocks for KV head h (float64, host)."""

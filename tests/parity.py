@@ -49,6 +49,7 @@ class Report:
     max_dense_err: float = 0.0
     max_recon_rel: float = 0.0
     max_sigma_rel: float = 0.0
+    max_record_err: float = 0.0
     failures: List[str] = field(default_factory=list)
 
     def fail(self, msg):
@@ -204,9 +205,52 @@ def compare_dense_decode(layer, inputs, snap, res: O.UnitResult, rep: Report):
         rep.fail(f"dense lse b{b} h{h}: {np.abs(g_l - res.lse_dense).max():.3e}")
 
 
+def records_as_summaries(layer, inputs, b: int, h: int):
+    """The GPU-stored records of one unit's candidate pages as oracle page
+    summaries (values upcast exactly to fp64).  A bf16 record is a rounded
+    copy of the spectral summary, so its selection and score gates take the
+    oracle scoring the stored record itself; only mu, V and C enter a score."""
+    w = inputs.workload
+    _, cand = O.forced_and_candidates(int(inputs.seq_lens[b]), w.page_size)
+    if len(cand) == 0:
+        return {}
+    pages = [int(j) for j in cand]
+    mu, V, C = layer.host_records(inputs.block_table[b, pages], h)
+    out = {}
+    for i, j in enumerate(pages):
+        sig = (C[i] ** 2).sum(axis=0)
+        out[j] = O.PageSummary(mu=mu[i], V=V[i], C=C[i], sigma2=sig, tau=0.0,
+                               kept=int((sig > 0).sum()))
+    return out
+
+
+def record_error(layer, inputs, b: int, h: int, fp64) -> float:
+    """Max over the unit's pages of |C V^T (stored) - C V^T (fp64)| / max|D|:
+    how far a reduced-precision record is from the fp64 summary (a measurement,
+    not a gate)."""
+    w = inputs.workload
+    pages = sorted(fp64)
+    if not pages:
+        return 0.0
+    _, V, C = layer.host_records(inputs.block_table[b, pages], h)
+    err = 0.0
+    for i, j in enumerate(pages):
+        s = fp64[j]
+        if degenerate(s, w.rank):
+            continue                      # no unique rank-r subspace to compare
+        keys = O.page_keys(inputs.k_cache, inputs.block_table, b, h, j, w.page_size)
+        scale = np.abs(keys - keys.mean(axis=0)).max()
+        err = max(err, float(np.abs(C[i] @ V[i].T - s.C @ s.V.T).max() / scale))
+    return err
+
+
 def run_case(inputs, units=None, dense=True, check_build=True, summary_dtype=0):
     """Build, select, sparse- and dense-decode on the GPU; compare the given
-    units (default: all) with the oracle.  Returns (report, layer, snapshot)."""
+    units (default: all) with the oracle.  Returns (report, layer, snapshot).
+
+    summary_dtype 1 (bf16 records): the build is measured, not gated
+    (report.max_record_err), and selection/scores are gated against the oracle
+    scoring the GPU-stored records."""
     import torch
     from sparse_paged_kv_gb300 import runtime
     w = inputs.workload
@@ -234,9 +278,15 @@ def run_case(inputs, units=None, dense=True, check_build=True, summary_dtype=0):
     if units is None:
         units = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
     for b, h in units:
+        stored = records_as_summaries(layer, inputs, b, h) if summary_dtype == 1 else None
         res = O.run_unit(inputs.q, inputs.k_cache, inputs.v_cache, inputs.block_table,
-                         inputs.seq_lens, w.n_kv_heads, w.rank, w.budget_tokens, b, h, dense=dense)
-        if check_build:
+                         inputs.seq_lens, w.n_kv_heads, w.rank, w.budget_tokens, b, h, dense=dense,
+                         summaries=stored)
+        if check_build and summary_dtype == 1:
+            fp64 = O.build_unit(inputs.k_cache, inputs.block_table, int(inputs.seq_lens[b]), b, h,
+                                w.rank)
+            rep.max_record_err = max(rep.max_record_err, record_error(layer, inputs, b, h, fp64))
+        elif check_build:
             compare_build(layer, inputs, res, rep, tail=tail_h, block_index=block_index)
         compare_select(layer, snap, res, rep)
         compare_sparse_decode(layer, inputs, snap, res, rep)

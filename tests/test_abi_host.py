@@ -55,6 +55,8 @@ def test_record_bytes(lib):
     assert B.summary_record_bytes(cfg(rank=15)) == ((16 + 1) * 128 + 16 * 64) * 4
     assert B.summary_record_bytes(cfg(head_dim=64)) == 0          # unsupported
     assert B.summary_record_bytes(cfg(n_q_heads=6, n_kv_heads=2)) == 0   # G = 3
+    for c in (cfg(), cfg(summary_dtype=B.LOCKS_SUMMARY_BF16), cfg(rank=15), cfg(head_dim=64)):
+        assert lib.locks_summary_bytes(ctypes.byref(c.c())) == B.summary_record_bytes(c)
 
 
 def test_workspace_sizes_grow_with_shape(lib):

@@ -51,3 +51,19 @@ def test_full_size(name):
     print(f"{name}: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} dense "
           f"{rep.max_dense_err:.2e} recon {rep.max_recon_rel:.2e} degenerate {rep.degenerate} "
           f"ties {rep.tie_diffs}")
+
+
+def test_full_size_bf16_records():
+    """llama32k with bf16 summary records, two sampled units end to end."""
+    import torch
+    w = W.get("llama32k")
+    inputs = W.generate(w)
+    rep, layer, snap = P.run_case(inputs, units=[(0, 0), (w.batch - 1, w.n_kv_heads - 1)],
+                                  dense=False, summary_dtype=1)
+    rep.check()
+    assert snap["status"] == 0
+    assert rep.max_record_err < 2e-2, rep.max_record_err
+    del layer
+    torch.cuda.empty_cache()
+    print(f"llama32k bf16: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} record vs fp64 "
+          f"{rep.max_record_err:.2e} ties {rep.tie_diffs}")

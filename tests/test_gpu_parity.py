@@ -1,8 +1,11 @@
 """CUDA path against the fp64 oracle on small seeded workloads (several tiles,
 ragged tails, GQA group sizes 1..8, ranks 4..16, the degenerate cases)."""
+import dataclasses
+
 import numpy as np
 import pytest
 
+import oracle as O
 import workloads as W
 from tests import parity as P
 
@@ -54,6 +57,23 @@ def test_parity(name):
     print(f"{name}: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} dense "
           f"{rep.max_dense_err:.2e} recon {rep.max_recon_rel:.2e} sigma {rep.max_sigma_rel:.2e} "
           f"degenerate {rep.degenerate} ties {rep.tie_diffs}")
+
+
+BF16_CASES = ["tiny", "ragged", "group8", "rank16", "multichunk", "slices3", "k40"]
+
+
+@pytest.mark.parametrize("name", BF16_CASES)
+def test_parity_bf16_records(name):
+    """bf16 summary records: selection and scores against the oracle scoring the
+    stored records; decode as for fp32; record error against fp64 reported."""
+    inputs = W.generate(CASES[name])
+    rep, layer, snap = P.run_case(inputs, summary_dtype=1)
+    rep.check()
+    assert rep.units == CASES[name].batch * CASES[name].n_kv_heads
+    # bf16 keeps 8 significant bits: the stored C V^T is a rounded copy
+    assert rep.max_record_err < 2e-2, rep.max_record_err
+    print(f"bf16 {name}: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} record vs fp64 "
+          f"{rep.max_record_err:.2e} ties {rep.tie_diffs}")
 
 
 def test_empty_sequence_outputs_zero():
@@ -116,3 +136,40 @@ def test_jacobi_sweep_cap_is_flagged():
     torch.cuda.synchronize()
     s = st.cpu().numpy()
     assert np.all((s >> 16) == 0) and np.all((s & 0xFFFF) <= 20)
+
+
+def test_graph_replay_matches_eager_and_oracle():
+    """A captured step replays bit-identically to the eager calls, reads q at
+    replay time, and still passes the oracle gates with a new q."""
+    import torch
+    inputs = W.generate(CASES["batch_heads"])
+    rep, layer, snap = P.run_case(inputs, dense=False, check_build=False)
+    rep.check()
+    graph = layer.capture_step()
+    rng = np.random.default_rng(77)
+    for trial in range(2):
+        q_new = W.f32_to_bf16_bits(rng.standard_normal(inputs.q.shape).astype(np.float32))
+        layer.q.copy_(torch.from_numpy(q_new.view(np.int16)).view(layer.q.dtype).cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        sel_g = layer.selected.cpu().numpy().copy()
+        out_g = layer.out.float().cpu().numpy().copy()
+        lse_g = layer.out_lse.cpu().numpy().copy()
+        layer.step()
+        torch.cuda.synchronize()
+        assert np.array_equal(sel_g, layer.selected.cpu().numpy())
+        assert np.array_equal(out_g, layer.out.float().cpu().numpy())
+        assert np.array_equal(lse_g, layer.out_lse.cpu().numpy())
+        # the replayed result against the oracle on the new query
+        inputs2 = dataclasses.replace(inputs, q=q_new)
+        snap2 = {"selected": sel_g, "out": out_g.astype(np.float64),
+                 "out_lse": lse_g.astype(np.float64)}
+        rep2 = P.Report()
+        w = inputs.workload
+        for b, h in [(0, 0), (w.batch - 1, w.n_kv_heads - 1)]:
+            res = O.run_unit(inputs2.q, inputs2.k_cache, inputs2.v_cache, inputs2.block_table,
+                             inputs2.seq_lens, w.n_kv_heads, w.rank, w.budget_tokens, b, h)
+            P.compare_select(layer, snap2, res, rep2)
+            P.compare_sparse_decode(layer, inputs2, snap2, res, rep2)
+        rep2.check()
+    assert int(layer.status.cpu()[0]) == 0
