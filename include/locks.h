@@ -38,8 +38,8 @@
  *    the same workspace can be replayed inside a CUDA graph.  Calls that share
  *    a workspace must not overlap on the GPU.
  *
- * Supported shapes: head_dim = 128; page_size = 64; 1 <= rank <= 16; G in
- * {1, 2, 4, 8}.  Other values return LOCKS_ERR_UNSUPPORTED.
+ * Supported shapes: head_dim = 128; page_size = 64 or 16; 1 <= rank <= 16;
+ * G in {1, 2, 4, 8}.  Other values return LOCKS_ERR_UNSUPPORTED.
  */
 #ifndef LOCKS_H_
 #define LOCKS_H_

@@ -13,7 +13,6 @@
 namespace {
 
 using locks::kHeadDim;
-using locks::kPageSize;
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -28,7 +27,8 @@ int check_cfg(const locks_cfg_t* c) {
   if (c->n_q_heads % c->n_kv_heads != 0) return LOCKS_ERR_INVALID_ARG;
   if (c->summary_dtype != LOCKS_SUMMARY_F32 && c->summary_dtype != LOCKS_SUMMARY_BF16)
     return LOCKS_ERR_INVALID_ARG;
-  if (c->head_dim != kHeadDim || c->page_size != kPageSize) return LOCKS_ERR_UNSUPPORTED;
+  if (c->head_dim != kHeadDim || (c->page_size != 64 && c->page_size != 16))
+    return LOCKS_ERR_UNSUPPORTED;
   if (c->rank > 16) return LOCKS_ERR_UNSUPPORTED;
   if (!is_pow2_group(c->n_q_heads / c->n_kv_heads)) return LOCKS_ERR_UNSUPPORTED;
   return LOCKS_OK;
@@ -52,7 +52,7 @@ DecodeLayout decode_layout(const locks_cfg_t* c, int n_pages) {
   DecodeLayout L;
   const int G = group_of(c);
   const size_t U = size_t(c->batch) * c->n_kv_heads;
-  L.pages_per_split = locks::decode_pages_per_split(long(U), n_pages);
+  L.pages_per_split = locks::decode_pages_per_split(long(U), n_pages, c->page_size);
   L.n_splits_max = n_pages > 0 ? (n_pages + L.pages_per_split - 1) / L.pages_per_split : 1;
   L.part = 0;
   L.ticket = align_up(U * L.n_splits_max * G * locks::kPartStride * sizeof(float));
@@ -77,14 +77,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A KV pool viewed as a 2-D bf16 tensor of (num_blocks * n_kv_heads * B) rows
-// of head_dim elements, read in 64 x 64 boxes with 128-byte swizzle.
+// of head_dim elements, read in boxes of B rows x 64 columns (one page-head's
+// half rows) with 128-byte swizzle.
 bool encode_pool_map(CUtensorMap* m, const void* pool, const locks_cfg_t* c) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cuuint64_t(c->head_dim),
                               cuuint64_t(c->num_blocks) * c->n_kv_heads * c->page_size};
   const cuuint64_t strides[1] = {cuuint64_t(c->head_dim) * 2};
-  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t box[2] = {64, cuuint32_t(c->page_size)};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -118,6 +119,7 @@ int decode_common(const locks_cfg_t* cfg, const void* q, const void* k_cache, co
   p.n_kv_heads = cfg->n_kv_heads;
   p.max_pages = cfg->max_pages;
   p.num_blocks = cfg->num_blocks;
+  p.page_size = cfg->page_size;
   p.k = k;
   p.pages_per_split = L.pages_per_split;
   p.n_splits_max = L.n_splits_max;
@@ -179,7 +181,7 @@ int locks_build_summaries(const locks_cfg_t* cfg, const void* k_cache, const int
   p.num_blocks = cfg->num_blocks;
   p.rank = cfg->rank;
   p.max_sweeps = max_sweeps == 0 ? 20 : max_sweeps;
-  return locks::launch_build(p, locks::rank_cap(cfg->rank), cfg->summary_dtype,
+  return locks::launch_build(p, locks::rank_cap(cfg->rank), cfg->summary_dtype, cfg->page_size,
                              static_cast<cudaStream_t>(stream));
 }
 
@@ -217,6 +219,7 @@ int locks_select(const locks_cfg_t* cfg, const void* q, const void* summaries,
   p.n_kv_heads = cfg->n_kv_heads;
   p.max_pages = cfg->max_pages;
   p.num_blocks = cfg->num_blocks;
+  p.page_size = cfg->page_size;
   p.k = k;
   p.mc = L.mc;
   p.per_cta = L.per_cta;

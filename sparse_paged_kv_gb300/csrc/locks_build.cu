@@ -2,12 +2,12 @@
 // "Locks: Page-Local Compact Key Summaries for Efficient Long-Context
 // Decoding", section 4 "Build" (and the blog review's Algorithm 1).
 //
-// One CTA of 256 threads per (block, KV head) page:
-//   1. load the page's B = 64 bf16 keys, mu = mean of the keys, D = K - mu (fp32);
-//   2. Gram A = D D^T (64 x 64), 4 x 4 register tiles per thread;
-//   3. parallel cyclic Jacobi: each sweep is 63 rounds of 32 disjoint
+// One CTA of 256 threads per (block, KV head) page, page size B = 64 or 16:
+//   1. load the page's B bf16 keys, mu = mean of the keys, D = K - mu (fp32);
+//   2. Gram A = D D^T (B x B), (B/16) x (B/16) register tiles per thread;
+//   3. parallel cyclic Jacobi: each sweep is B-1 rounds of B/2 disjoint
 //      (p, q) rotations (round-robin ordering, so every pair meets once per
-//      sweep); a round applies A <- J^T A J as 1024 independent 2 x 2 block
+//      sweep); a round applies A <- J^T A J as (B/2)^2 independent 2 x 2 block
 //      transforms and U <- U J; sweeps stop when the off-diagonal Frobenius
 //      norm falls below 1e-6 of the total (or at max_sweeps, flagged);
 //   4. the top-r eigenpairs in descending order (ties: lower index); modes
@@ -24,17 +24,18 @@ namespace {
 
 constexpr int kBuildThreads = 256;
 constexpr int kDS = kHeadDim + 4;   // padded row stride of D (floats)
-constexpr int kAS = kPageSize + 1;  // padded row stride of A and U
 constexpr float kJacobiTol = 1e-6f;
 constexpr float kDropRel = 1e-5f;
 
+template <int PB>
 struct BuildSmem {
-  float D[kPageSize * kDS];
-  float A[kPageSize * kAS];
-  float U[kPageSize * kAS];
+  static constexpr int AS = PB + 1;   // padded row stride of A and U
+  float D[PB * kDS];
+  float A[PB * AS];
+  float U[PB * AS];
   float mu[kHeadDim];
-  float rot_c[32], rot_s[32];
-  int rot_p[32], rot_q[32];
+  float rot_c[PB / 2], rot_s[PB / 2];
+  int rot_p[PB / 2], rot_q[PB / 2];
   float red[kBuildThreads / 32 * 2];
   float lam[16];
   int order[16];
@@ -42,19 +43,24 @@ struct BuildSmem {
   int flag;
 };
 
+// round k's pair t of the circle method on PB players: player PB-1 fixed, the
+// other PB-1 rotate
+template <int PB>
 __device__ __forceinline__ void round_pair(int t, int k, int& p, int& q) {
-  // circle method on 64 players: player 63 fixed, the other 63 rotate
   int a, b;
-  if (k == 0) { a = t; b = kPageSize - 1; }
-  else { a = (t + k) % (kPageSize - 1); b = (t - k + (kPageSize - 1)) % (kPageSize - 1); }
+  if (k == 0) { a = t; b = PB - 1; }
+  else { a = (t + k) % (PB - 1); b = (t - k + (PB - 1)) % (PB - 1); }
   p = min(a, b);
   q = max(a, b);
 }
 
-template <int RP, typename T>
+template <int RP, typename T, int PB>
 __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams prm) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  BuildSmem& S = *reinterpret_cast<BuildSmem*>(smem_raw);
+  BuildSmem<PB>& S = *reinterpret_cast<BuildSmem<PB>*>(smem_raw);
+  constexpr int kAS = BuildSmem<PB>::AS;
+  constexpr int NPR = PB / 2;          // rotations per round
+  constexpr int TT = PB / 16;          // Gram register tile edge
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int pid = blockIdx.x;
   const int h = blockIdx.y;
@@ -67,9 +73,9 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
 
   // ---- 1. keys -> D, mu ----------------------------------------------------
   const uint4* src = reinterpret_cast<const uint4*>(
-      prm.k_cache + (size_t(blk) * prm.n_kv_heads + h) * (kPageSize * kHeadDim));
+      prm.k_cache + (size_t(blk) * prm.n_kv_heads + h) * (PB * kHeadDim));
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < PB / 16; ++e) {
     const int idx = tid + kBuildThreads * e;       // 16-byte chunk of the 16 KiB page
     const int row = idx >> 4, col = (idx & 15) * 8;
     const uint4 w = src[idx];
@@ -80,11 +86,11 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   __syncthreads();
   if (tid < kHeadDim) {
     float s = 0.f;
-    for (int i = 0; i < kPageSize; ++i) s += S.D[i * kDS + tid];
-    S.mu[tid] = s * (1.f / kPageSize);
+    for (int i = 0; i < PB; ++i) s += S.D[i * kDS + tid];
+    S.mu[tid] = s * (1.f / PB);
   }
   __syncthreads();
-  for (int idx = tid; idx < kPageSize * kHeadDim; idx += kBuildThreads) {
+  for (int idx = tid; idx < PB * kHeadDim; idx += kBuildThreads) {
     const int i = idx >> 7, t = idx & 127;
     S.D[i * kDS + t] -= S.mu[t];
   }
@@ -93,28 +99,28 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   // ---- 2. Gram A = D D^T: thread (ti, tj) owns rows ti+16a, cols tj+16b ----
   {
     const int ti = tid >> 4, tj = tid & 15;
-    float acc[4][4] = {};
+    float acc[TT][TT] = {};
     for (int c = 0; c < kHeadDim; c += 4) {
-      float4 di[4], dj[4];
+      float4 di[TT], dj[TT];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
+      for (int a = 0; a < TT; ++a) {
         di[a] = *reinterpret_cast<const float4*>(S.D + (ti + 16 * a) * kDS + c);
         dj[a] = *reinterpret_cast<const float4*>(S.D + (tj + 16 * a) * kDS + c);
       }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < TT; ++a)
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb)
+        for (int bb = 0; bb < TT; ++bb)
           acc[a][bb] += di[a].x * dj[bb].x + di[a].y * dj[bb].y + di[a].z * dj[bb].z +
                         di[a].w * dj[bb].w;
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < TT; ++a)
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) S.A[(ti + 16 * a) * kAS + tj + 16 * bb] = acc[a][bb];
+      for (int bb = 0; bb < TT; ++bb) S.A[(ti + 16 * a) * kAS + tj + 16 * bb] = acc[a][bb];
   }
-  for (int idx = tid; idx < kPageSize * kPageSize; idx += kBuildThreads) {
-    const int i = idx >> 6, j = idx & 63;
+  for (int idx = tid; idx < PB * PB; idx += kBuildThreads) {
+    const int i = idx / PB, j = idx % PB;
     S.U[i * kAS + j] = (i == j) ? 1.f : 0.f;
   }
   __syncthreads();
@@ -125,8 +131,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   for (;;) {
     // off-diagonal and total Frobenius norms
     float off = 0.f, tot = 0.f;
-    for (int idx = tid; idx < kPageSize * kPageSize; idx += kBuildThreads) {
-      const int i = idx >> 6, j = idx & 63;
+    for (int idx = tid; idx < PB * PB; idx += kBuildThreads) {
+      const int i = idx / PB, j = idx % PB;
       const float a = S.A[i * kAS + j];
       tot += a * a;
       if (i != j) off += a * a;
@@ -144,10 +150,10 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     if (S.flag) { converged = true; break; }
     if (sweeps >= prm.max_sweeps) break;
     ++sweeps;
-    for (int r = 0; r < kPageSize - 1; ++r) {
-      if (tid < 32) {
+    for (int r = 0; r < PB - 1; ++r) {
+      if (tid < NPR) {
         int p, q;
-        round_pair(r, tid, p, q);
+        round_pair<PB>(r, tid, p, q);
         const float app = S.A[p * kAS + p], aqq = S.A[q * kAS + q], apq = S.A[p * kAS + q];
         float c = 1.f, s = 0.f;
         if (apq != 0.f) {
@@ -161,13 +167,14 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
         S.rot_c[tid] = c; S.rot_s[tid] = s; S.rot_p[tid] = p; S.rot_q[tid] = q;
       }
       __syncthreads();
-      {
+      if (NPR * NPR >= kBuildThreads || tid < NPR * NPR) {
         // 2 x 2 blocks (K, L): rows (pK, qK), cols (pL, qL); B'' = J_K^T B J_L
+        // (B = 64: thread owns K = tid / 8 and L = tid % 8 + 8m; B = 16: one block)
         const int K = tid >> 3;
         const float cK = S.rot_c[K], sK = S.rot_s[K];
         const int pK = S.rot_p[K], qK = S.rot_q[K];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < (NPR * NPR + kBuildThreads - 1) / kBuildThreads; ++m) {
           const int L = (tid & 7) + 8 * m;
           const float cL = S.rot_c[L], sL = S.rot_s[L];
           const int pL = S.rot_p[L], qL = S.rot_q[L];
@@ -183,13 +190,16 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
           if (K == L) { n01 = 0.f; n10 = 0.f; }
           *a00 = n00; *a01 = n01; *a10 = n10; *a11 = n11;
         }
-        // U <- U J: pair L = tid & 31, rows (tid >> 5) + 8m
-        const int L = tid & 31;
+      }
+      // U <- U J: pair L = tid % NPR, rows tid / NPR + (256 / NPR) m
+      if (NPR * PB >= kBuildThreads || tid < NPR * PB) {
+        const int L = tid % NPR;
         const float cL = S.rot_c[L], sL = S.rot_s[L];
         const int pL = S.rot_p[L], qL = S.rot_q[L];
+        constexpr int RS = kBuildThreads / NPR;       // row step
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int i = (tid >> 5) + 8 * m;
+        for (int m = 0; m < (PB + RS - 1) / RS; ++m) {
+          const int i = tid / NPR + RS * m;
           const float up = S.U[i * kAS + pL], uq = S.U[i * kAS + qL];
           S.U[i * kAS + pL] = up * cL - uq * sL;
           S.U[i * kAS + qL] = up * sL + uq * cL;
@@ -202,8 +212,10 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   // ---- 4. top-r eigenpairs (warp 0), tau ------------------------------------
   const int r = prm.rank;
   if (warp == 0) {
-    float v0 = S.A[lane * kAS + lane], v1 = S.A[(lane + 32) * kAS + lane + 32];
-    bool t0 = false, t1 = false;
+    // lane holds diagonal entries lane and lane + 32 (those past B count as taken)
+    float v0 = lane < PB ? S.A[lane * kAS + lane] : 0.f;
+    float v1 = lane + 32 < PB ? S.A[(lane + 32) * kAS + lane + 32] : 0.f;
+    bool t0 = lane >= PB, t1 = lane + 32 >= PB;
     float lam1 = 0.f;
     for (int k = 0; k < r; ++k) {
       // candidate of this lane: larger value, ties -> lower index
@@ -241,7 +253,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     float v[RP];
 #pragma unroll
     for (int k = 0; k < RP; ++k) v[k] = 0.f;
-    for (int i = 0; i < kPageSize; ++i) {
+    for (int i = 0; i < PB; ++i) {
       const float dit = S.D[i * kDS + t];
 #pragma unroll
       for (int k = 0; k < RP; ++k)
@@ -254,11 +266,11 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     }
   } else {
     T* C = rec + rec_w_elems(RP);
-    for (int idx = tid - kHeadDim; idx < kPageSize * RP; idx += kBuildThreads - kHeadDim) {
+    for (int idx = tid - kHeadDim; idx < PB * RP; idx += kBuildThreads - kHeadDim) {
       const int i = idx / RP, k = idx % RP;
       const float lam = k < r ? S.lam[k] : 0.f;
       const float c = lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
-      st_elem(C + ((k >> 2) * kPageSize + i) * 4 + (k & 3), c);
+      st_elem(C + ((k >> 2) * PB + i) * 4 + (k & 3), c);
     }
   }
   if (tid == 0) {
@@ -267,10 +279,10 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   }
 }
 
-template <int RP, typename T>
+template <int RP, typename T, int PB>
 int launch_t(const BuildParams& p, cudaStream_t stream) {
-  const size_t smem = sizeof(BuildSmem);
-  auto kern = build_kernel<RP, T>;
+  const size_t smem = sizeof(BuildSmem<PB>);
+  auto kern = build_kernel<RP, T, PB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return LOCKS_ERR_CUDA;
@@ -278,16 +290,24 @@ int launch_t(const BuildParams& p, cudaStream_t stream) {
   return cudaPeekAtLastError() == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
 }
 
-}  // namespace
-
-int launch_build(const BuildParams& p, int RP, int dtype, cudaStream_t stream) {
-  const bool f32 = dtype == LOCKS_SUMMARY_F32;
+template <int PB>
+int launch_pb(const BuildParams& p, int RP, bool f32, cudaStream_t stream) {
   switch (RP) {
-    case 4: return f32 ? launch_t<4, float>(p, stream) : launch_t<4, __nv_bfloat16>(p, stream);
-    case 8: return f32 ? launch_t<8, float>(p, stream) : launch_t<8, __nv_bfloat16>(p, stream);
-    case 16: return f32 ? launch_t<16, float>(p, stream) : launch_t<16, __nv_bfloat16>(p, stream);
+    case 4: return f32 ? launch_t<4, float, PB>(p, stream) : launch_t<4, __nv_bfloat16, PB>(p, stream);
+    case 8: return f32 ? launch_t<8, float, PB>(p, stream) : launch_t<8, __nv_bfloat16, PB>(p, stream);
+    case 16:
+      return f32 ? launch_t<16, float, PB>(p, stream) : launch_t<16, __nv_bfloat16, PB>(p, stream);
     default: return LOCKS_ERR_UNSUPPORTED;
   }
+}
+
+}  // namespace
+
+int launch_build(const BuildParams& p, int RP, int dtype, int page_size, cudaStream_t stream) {
+  const bool f32 = dtype == LOCKS_SUMMARY_F32;
+  if (page_size == 64) return launch_pb<64>(p, RP, f32, stream);
+  if (page_size == 16) return launch_pb<16>(p, RP, f32, stream);
+  return LOCKS_ERR_UNSUPPORTED;
 }
 
 }  // namespace locks

@@ -18,7 +18,6 @@
 namespace locks {
 
 constexpr int kHeadDim = 128;
-constexpr int kPageSize = 64;
 constexpr unsigned kFull = 0xffffffffu;
 // A bounded wait on a copy gives up after this many nanoseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

@@ -41,7 +41,8 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
-constexpr int kTokPerWarp = kPageSize / kConsumerWarps;    // 16
+constexpr int kTokPerWarp = 16;                            // tokens per consumer warp per stage
+constexpr int kStageTokens = kConsumerWarps * kTokPerWarp; // 64
 constexpr int kBoxBytes = 64 * 128;                        // 64 rows x 64 bf16
 constexpr int kSlotBytes = 4 * kBoxBytes;                  // K0 K1 V0 V1 (32 KiB)
 constexpr int kMaxPagesPerSplit = 256;
@@ -139,7 +140,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk) {
   return box + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <int G, int STAGES, bool CLUSTERED>
+template <int G, int STAGES, bool CLUSTERED, int PB>
 __global__ void __launch_bounds__(kDecThreads)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v) {
@@ -147,14 +148,15 @@ __global__ void __launch_bounds__(kDecThreads)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
   const int u = blockIdx.y, sp = blockIdx.x;
   const int b = u / p.n_kv_heads, h = u % p.n_kv_heads;
-  constexpr int B = kPageSize;
+  constexpr int B = PB;
+  constexpr int PPS = kStageTokens / PB;   // pages per ring stage (1 or 4)
 
   // ---- shared memory ------------------------------------------------------
   unsigned char* ring = smem;                                       // STAGES x 32 KiB
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(STAGES) * kSlotBytes);
   uint64_t* empty = full + STAGES;
-  int* slot_nv = reinterpret_cast<int*>(empty + STAGES);
-  float* wstate = reinterpret_cast<float*>(slot_nv + 4);            // [4][2G]
+  int* slot_nv = reinterpret_cast<int*>(empty + STAGES);            // [STAGES][4] per warp
+  float* wstate = reinterpret_cast<float*>(slot_nv + 4 * STAGES);   // [4][2G]
   __shared__ int s_blk[kMaxPagesPerSplit], s_nv[kMaxPagesPerSplit];
   __shared__ int s_is_last;
 
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kDecThreads)
   if (!CLUSTERED && sp >= nsplits) return;
   const int i_lo = sp * p.pages_per_split;
   const int cnt = max(0, min(n_list, i_lo + p.pages_per_split) - i_lo);
-
+  const int nst = (cnt + PPS - 1) / PPS;   // ring stages of this split
   // page ids of this split: block and valid tokens, checked once
   const int32_t* bt = p.block_table + size_t(b) * p.max_pages;
   for (int t = tid; t < cnt; t += kDecThreads) {
@@ -228,22 +230,47 @@ __global__ void __launch_bounds__(kDecThreads)
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      for (int i = 0; i < cnt; ++i) {
+      for (int i = 0; i < nst; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES && !mbar_wait_bounded(empty + s, ((i / STAGES) - 1) & 1)) {
           flag_status(p.status, LOCKS_DEV_WAIT_TIMEOUT);
           break;
         }
-        const int nv = s_nv[i], blk = s_blk[i];
-        slot_nv[s] = nv;
-        if (nv > 0) {
-          const int row = (blk * p.n_kv_heads + h) * B;
-          unsigned char* slot = ring + size_t(s) * kSlotBytes;
-          mbar_arrive_expect_tx(full + s, kSlotBytes);
-          tma_load_2d(slot, &tmap_k, 0, row, full + s);
-          tma_load_2d(slot + kBoxBytes, &tmap_k, 64, row, full + s);
-          tma_load_2d(slot + 2 * kBoxBytes, &tmap_v, 0, row, full + s);
-          tma_load_2d(slot + 3 * kBoxBytes, &tmap_v, 64, row, full + s);
+        // a stage is 64 token rows: one page (B = 64) or four (B = 16); warp w
+        // attends rows [16w, 16w + 16), i.e. its valid count is per warp
+        unsigned char* slot = ring + size_t(s) * kSlotBytes;
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int e = 0; e < PPS; ++e) {
+          const int t = i * PPS + e;
+          if (t < cnt && s_nv[t] > 0) bytes += 2u * PB * kHeadDim * 2u;
+        }
+        if (PPS == 1) {
+          const int nv = s_nv[i];
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w)
+            slot_nv[s * 4 + w] = min(kTokPerWarp, max(0, nv - w * kTokPerWarp));
+        } else {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const int t = i * PPS + w;
+            slot_nv[s * 4 + w] = t < cnt ? s_nv[t] : 0;
+          }
+        }
+        if (bytes) {
+          mbar_arrive_expect_tx(full + s, bytes);
+#pragma unroll
+          for (int e = 0; e < PPS; ++e) {
+            const int t = i * PPS + e;
+            if (t < cnt && s_nv[t] > 0) {
+              const int row = (s_blk[t] * p.n_kv_heads + h) * B;
+              unsigned char* dst = slot + e * PB * 128;   // rows [PB e, PB e + PB) of each box
+              tma_load_2d(dst, &tmap_k, 0, row, full + s);
+              tma_load_2d(dst + kBoxBytes, &tmap_k, 64, row, full + s);
+              tma_load_2d(dst + 2 * kBoxBytes, &tmap_v, 0, row, full + s);
+              tma_load_2d(dst + 3 * kBoxBytes, &tmap_v, 64, row, full + s);
+            }
+          }
         } else {
           mbar_arrive(full + s);
         }
@@ -262,9 +289,9 @@ __global__ void __launch_bounds__(kDecThreads)
       }
     }
     const int n0 = warp * kTokPerWarp;
-    int done = cnt;
+    int done = nst;
     bool aborted = false;
-    for (int i = 0; i < cnt; ++i) {
+    for (int i = 0; i < nst; ++i) {
       const int s = i % STAGES;
       if (!__all_sync(kFull, mbar_wait_bounded(full + s, (i / STAGES) & 1))) {
         if (lane == 0) flag_status(p.status, LOCKS_DEV_WAIT_TIMEOUT);
@@ -272,8 +299,8 @@ __global__ void __launch_bounds__(kDecThreads)
         done = i;
         break;
       }
-      const int nv = slot_nv[s];
-      if (nv > n0) {
+      const int nv = slot_nv[s * 4 + warp];   // valid rows among this warp's 16
+      if (nv > 0) {
         const uint32_t kbox = smem_u32(ring + size_t(s) * kSlotBytes);
         const uint32_t vbox = kbox + 2 * kBoxBytes;
         // ---- S = Q K^T over this warp's 16 tokens (two 8-token tiles) ----
@@ -289,8 +316,8 @@ __global__ void __launch_bounds__(kDecThreads)
             mma16816(sacc[1], qa0[ks], 0u, qa2[ks], 0u, kb[2], kb[3]);
           }
         }
-        // ---- online softmax for head g over tokens n0 + {2t, 2t+1, 8+2t, 9+2t} ----
-        const int tk0 = n0 + 2 * t4;
+        // ---- online softmax for head g over rows n0 + {2t, 2t+1, 8+2t, 9+2t} ----
+        const int tk0 = 2 * t4;
         float sv[4] = {sacc[0][0], sacc[0][1], sacc[1][0], sacc[1][1]};
         const int tks[4] = {tk0, tk0 + 1, tk0 + 8, tk0 + 9};
         float mt = -INFINITY;
@@ -319,8 +346,8 @@ __global__ void __launch_bounds__(kDecThreads)
         }
         const uint32_t pa0 = pack_bf16(pr[0], pr[1]), pa2 = pack_bf16(pr[2], pr[3]);
         // ---- tokens past the valid count: zero their V rows (never 0 x NaN) ----
-        if (nv < n0 + kTokPerWarp) {
-          for (int r = max(nv, n0); r < n0 + kTokPerWarp; ++r) {
+        if (nv < kTokPerWarp) {
+          for (int r = n0 + nv; r < n0 + kTokPerWarp; ++r) {
             unsigned char* row0 = ring + size_t(s) * kSlotBytes + 2 * kBoxBytes + r * 128;
             if (lane < 8) *reinterpret_cast<uint4*>(row0 + lane * 16) = make_uint4(0, 0, 0, 0);
             else if (lane < 16)
@@ -346,7 +373,7 @@ __global__ void __launch_bounds__(kDecThreads)
       if (lane == 0) mbar_arrive(empty + s);
     }
     if (aborted) {
-      for (int i = done; i < min(cnt, done + STAGES); ++i)
+      for (int i = done; i < min(nst, done + STAGES); ++i)
         mbar_wait_bounded(full + (i % STAGES), (i / STAGES) & 1);
     }
   }
@@ -481,20 +508,20 @@ __global__ void __launch_bounds__(kDecThreads)
 
 template <int G>
 constexpr size_t decode_smem_bytes(int stages) {
-  return size_t(stages) * kSlotBytes + 2 * stages * sizeof(uint64_t) + 4 * sizeof(int) +
+  return size_t(stages) * kSlotBytes + 2 * stages * sizeof(uint64_t) + 4 * stages * sizeof(int) +
          kConsumerWarps * 2 * G * sizeof(float);
 }
 
 // Whether clusters of C decode CTAs can be resident on this device (queried
 // once per group size and cluster size).
-template <int G>
+template <int G, int PB>
 bool cluster_fits(int C) {
   static int known[kMaxClusterSplits + 1] = {};   // 0 unknown, 1 yes, -1 no
   if (C < 1 || C > kMaxClusterSplits) return false;
   int k = __atomic_load_n(&known[C], __ATOMIC_ACQUIRE);
   if (k != 0) return k > 0;
   constexpr int STAGES = 3;
-  auto kern = decode_kernel<G, STAGES, true>;
+  auto kern = decode_kernel<G, STAGES, true, PB>;
   const size_t smem = decode_smem_bytes<G>(STAGES);
   bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) ==
                 cudaSuccess &&
@@ -520,12 +547,12 @@ bool cluster_fits(int C) {
   return ok;
 }
 
-template <int G>
+template <int G, int PB>
 int launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int gx, int gy,
              bool clustered, cudaStream_t stream) {
   constexpr int STAGES = 3;
   const size_t smem = decode_smem_bytes<G>(STAGES);
-  auto kern = clustered ? decode_kernel<G, STAGES, true> : decode_kernel<G, STAGES, false>;
+  auto kern = clustered ? decode_kernel<G, STAGES, true, PB> : decode_kernel<G, STAGES, false, PB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return LOCKS_ERR_CUDA;
@@ -546,45 +573,57 @@ int launch_g(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv
   return cudaLaunchKernelEx(&lc, kern, p, tk, tv) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
 }
 
-template <int G>
+template <int G, int PB>
 int launch_list(DecodeParams p, const CUtensorMap& tk, const CUtensorMap& tv, int gx, int gy,
                 cudaStream_t stream) {
   if (p.selected && p.k > 0) {
-    // equal-length lists: one cluster of at most kMaxClusterSplits splits per unit
-    const int pps = std::max(p.pages_per_split, (p.k + kMaxClusterSplits - 1) / kMaxClusterSplits);
+    // equal-length lists: one cluster of at most kMaxClusterSplits splits per
+    // unit, each split a whole number of ring stages
+    constexpr int PPS = kStageTokens / PB;
+    int pps = std::max(p.pages_per_split, (p.k + kMaxClusterSplits - 1) / kMaxClusterSplits);
+    pps = (pps + PPS - 1) / PPS * PPS;
     const int C = (p.k + pps - 1) / pps;
-    if (cluster_fits<G>(C)) {
+    if (cluster_fits<G, PB>(C)) {
       p.pages_per_split = pps;
-      return launch_g<G>(p, tk, tv, C, gy, true, stream);
+      return launch_g<G, PB>(p, tk, tv, C, gy, true, stream);
     }
   }
-  return launch_g<G>(p, tk, tv, gx, gy, false, stream);
+  return launch_g<G, PB>(p, tk, tv, gx, gy, false, stream);
+}
+
+template <int PB>
+int launch_pb(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int G, int gx,
+              int gy, cudaStream_t stream) {
+  switch (G) {
+    case 1: return launch_list<1, PB>(p, tk, tv, gx, gy, stream);
+    case 2: return launch_list<2, PB>(p, tk, tv, gx, gy, stream);
+    case 4: return launch_list<4, PB>(p, tk, tv, gx, gy, stream);
+    case 8: return launch_list<8, PB>(p, tk, tv, gx, gy, stream);
+    default: return LOCKS_ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace
 
-int decode_pages_per_split(long units, int n_pages) {
-  // a whole number of splits per unit such that all splits fit one wave of two
-  // CTAs per SM on 152 SMs (two waves for long page lists); at most
-  // kMaxPagesPerSplit pages per CTA
-  const long np = n_pages > 0 ? n_pages : 1;
+int decode_pages_per_split(long units, int n_pages, int page_size) {
+  // in ring stages of 64 tokens (one page of 64, four of 16): a whole number
+  // of splits per unit such that all splits fit one wave of two CTAs per SM on
+  // 152 SMs (two waves for long lists); at most kMaxPagesPerSplit pages per CTA
+  const long pps_stage = page_size > 0 && page_size < kStageTokens ? kStageTokens / page_size : 1;
+  const long np = n_pages > 0 ? (n_pages + pps_stage - 1) / pps_stage : 1;
   const long waves = units * np > 16384 ? 2 : 1;
   long splits = (waves * 2 * 152) / (units > 0 ? units : 1);
   if (splits < 1) splits = 1;
-  long pps = (np + splits - 1) / splits;
-  if (pps > kMaxPagesPerSplit) pps = kMaxPagesPerSplit;
-  return int(pps);
+  long st = (np + splits - 1) / splits;
+  if (st * pps_stage > kMaxPagesPerSplit) st = kMaxPagesPerSplit / pps_stage;
+  return int(st * pps_stage);
 }
 
 int launch_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int G,
                   int gx, int gy, cudaStream_t stream) {
-  switch (G) {
-    case 1: return launch_list<1>(p, tk, tv, gx, gy, stream);
-    case 2: return launch_list<2>(p, tk, tv, gx, gy, stream);
-    case 4: return launch_list<4>(p, tk, tv, gx, gy, stream);
-    case 8: return launch_list<8>(p, tk, tv, gx, gy, stream);
-    default: return LOCKS_ERR_UNSUPPORTED;
-  }
+  if (p.page_size == 64) return launch_pb<64>(p, tk, tv, G, gx, gy, stream);
+  if (p.page_size == 16) return launch_pb<16>(p, tk, tv, G, gx, gy, stream);
+  return LOCKS_ERR_UNSUPPORTED;
 }
 
 }  // namespace locks

@@ -29,6 +29,7 @@ struct SelectParams {
   int32_t* ws_ticket;            // [U]
   size_t rec_bytes;
   int units, n_kv_heads, max_pages, num_blocks;
+  int page_size;                 // tokens per page B (64 or 16)
   int k;                         // page budget
   int mc, per_cta, nseg_max;     // score kernel geometry (see select_geometry)
   int slice, nslices_max, fin_cap, cand_per_slice;
@@ -62,6 +63,7 @@ struct DecodeParams {
   float* ws_part;                // [U][n_splits_max][G][kPartStride]
   int32_t* ws_ticket;            // [U]
   int n_kv_heads, max_pages, num_blocks;
+  int page_size;                 // tokens per page B (64 or 16)
   int k;                         // row stride of `selected`
   int pages_per_split, n_splits_max;
   float scale, scale_log2;
@@ -78,11 +80,17 @@ struct BuildParams {
 };
 
 SelectGeom select_geometry(int units, int max_pages, int G, int k);
+// score kernel only, one definition per page size (locks_select.cu: 64,
+// locks_score_b16.cu: 16)
+int launch_score_b64(const SelectParams& p, int G, int RP, int dtype, int n_ctas,
+                     cudaStream_t stream);
+int launch_score_b16(const SelectParams& p, int G, int RP, int dtype, int n_ctas,
+                     cudaStream_t stream);
 int launch_select(const SelectParams& p, int G, int RP, int dtype, int n_score_ctas,
                   int n_slices, cudaStream_t stream);
-int decode_pages_per_split(long units, int n_pages);
+int decode_pages_per_split(long units, int n_pages, int page_size);
 int launch_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int G,
                   int grid_x, int grid_y, cudaStream_t stream);
-int launch_build(const BuildParams& p, int RP, int dtype, cudaStream_t stream);
+int launch_build(const BuildParams& p, int RP, int dtype, int page_size, cudaStream_t stream);
 
 }  // namespace locks

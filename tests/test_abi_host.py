@@ -54,6 +54,9 @@ def test_record_bytes(lib):
     assert B.summary_record_bytes(cfg(rank=3)) == ((4 + 1) * 128 + 4 * 64) * 4
     assert B.summary_record_bytes(cfg(rank=15)) == ((16 + 1) * 128 + 16 * 64) * 4
     assert B.summary_record_bytes(cfg(head_dim=64)) == 0          # unsupported
+    assert B.summary_record_bytes(cfg(page_size=16)) == ((8 + 1) * 128 + 8 * 16) * 4 == 5120
+    assert B.summary_record_bytes(cfg(page_size=16, rank=15)) == ((16 + 1) * 128 + 16 * 16) * 4
+    assert B.summary_record_bytes(cfg(page_size=32)) == 0
     assert B.summary_record_bytes(cfg(n_q_heads=6, n_kv_heads=2)) == 0   # G = 3
     for c in (cfg(), cfg(summary_dtype=B.LOCKS_SUMMARY_BF16), cfg(rank=15), cfg(head_dim=64)):
         assert lib.locks_summary_bytes(ctypes.byref(c.c())) == B.summary_record_bytes(c)
@@ -67,6 +70,8 @@ def test_workspace_sizes_grow_with_shape(lib):
     d = B.decode_workspace_bytes(cfg(), 64)
     assert 0 < s <= d
     assert B.decode_workspace_bytes(cfg(), -1) == 0
+    assert 0 < B.select_workspace_bytes(cfg(page_size=16), 512)
+    assert 0 < B.decode_workspace_bytes(cfg(page_size=16), 32)
 
 
 FAKE = 0x10000   # never dereferenced: every call below returns before a launch
@@ -85,7 +90,7 @@ def test_select_validation(lib):
     assert _select(lib, cfg(), ws_bytes=16) == B.LOCKS_ERR_WORKSPACE
     assert _select(lib, cfg(), q=None) == B.LOCKS_ERR_INVALID_ARG
     assert _select(lib, cfg(head_dim=96)) == B.LOCKS_ERR_UNSUPPORTED
-    assert _select(lib, cfg(page_size=16)) == B.LOCKS_ERR_UNSUPPORTED
+    assert _select(lib, cfg(page_size=32)) == B.LOCKS_ERR_UNSUPPORTED     # B in {64, 16}
     assert _select(lib, cfg(rank=17)) == B.LOCKS_ERR_UNSUPPORTED
     assert _select(lib, cfg(n_q_heads=7)) == B.LOCKS_ERR_INVALID_ARG
     assert _select(lib, cfg(summary_dtype=5)) == B.LOCKS_ERR_INVALID_ARG

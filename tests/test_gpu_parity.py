@@ -36,6 +36,18 @@ CASES = {
     "k40": TINY.with_(context=64 * 300, budget_tokens=64 * 40, seed=2015),
     "k40_slices3": TINY.with_(context=64 * 4200, budget_tokens=64 * 40, global_rank=16,
                               seed=2016),
+    # page size 16 (four pages per decode stage)
+    "b16": TINY.with_(page_size=16, seed=2020),
+    "b16_ragged": TINY.with_(page_size=16, batch=5, seq_lens=(4096 + 7, 200, 16 * 33, 9, 0),
+                             seed=2021),
+    "b16_rank15": TINY.with_(page_size=16, rank=15, seed=2022),
+    "b16_slices2": TINY.with_(page_size=16, context=16 * 2500 + 5, global_rank=16,
+                              carrier_count=None, carrier_frac=0.01, seed=2023),
+    "b16_k40": TINY.with_(page_size=16, budget_tokens=16 * 40, seed=2025),
+    # Llama layer shape at B = 16: k = 128 (radix top-k, 16-split decode clusters)
+    "b16_gqa4_k128": TINY.with_(page_size=16, batch=2, n_q_heads=32, n_kv_heads=8,
+                                context=16384, budget_tokens=2048, global_rank=16,
+                                carrier_count=None, carrier_frac=0.01, seed=2024),
 }
 
 
@@ -59,7 +71,8 @@ def test_parity(name):
           f"degenerate {rep.degenerate} ties {rep.tie_diffs}")
 
 
-BF16_CASES = ["tiny", "ragged", "group8", "rank16", "multichunk", "slices3", "k40"]
+BF16_CASES = ["tiny", "ragged", "group8", "rank16", "multichunk", "slices3", "k40", "b16",
+              "b16_ragged"]
 
 
 @pytest.mark.parametrize("name", BF16_CASES)
