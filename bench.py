@@ -131,6 +131,15 @@ class ClockSampler:
                 "window": "timed region" if inside else "whole run (no sample inside the timed region)"}
 
 
+def source_digest(files) -> str:
+    """sha256 over the given repository files, concatenated in order."""
+    h = hashlib.sha256()
+    for rel in files:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profile_traffic(kernel_key: str, config: str):
     """DRAM bytes per launch of a kernel from the committed ncu summary, or None
     when the kernel source changed since the counters were taken."""
@@ -147,9 +156,8 @@ def profile_traffic(kernel_key: str, config: str):
     want = fields.get("source_sha256")
     if not src or not want:
         return None, path
-    with open(os.path.join(ROOT, src), "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != want:
-            return None, path
+    if source_digest([x.strip() for x in src.split(",")]) != want:
+        return None, path
     try:
         return float(fields["dram_bytes_per_launch"]), path
     except (KeyError, ValueError):
