@@ -48,6 +48,7 @@ constexpr int kBoxBytes = 64 * 128;                        // 64 rows x 64 bf16
 constexpr int kSlotBytes = 4 * kBoxBytes;                  // K0 K1 V0 V1 (32 KiB)
 constexpr int kMaxPagesPerSplit = 256;
 constexpr int kMaxClusterSplits = 16;                      // cluster size limit (non-portable above 8)
+constexpr int kMaxMergeCluster = 4;                        // largest cluster the sparse decode uses
 
 // float max through the integer atomics (ordering of IEEE bit patterns)
 __device__ __forceinline__ void atomicMax_float(float* addr, float v) {
@@ -471,14 +472,14 @@ constexpr size_t decode_smem_bytes(int stages) {
          kConsumerWarps * 2 * G * sizeof(float);
 }
 
-// Whether clusters of C decode CTAs can be resident on this device (queried
-// once per group size and cluster size).
+// How many clusters of C decode CTAs this device can hold at once (0: none;
+// queried once per group size, page size and cluster size).
 template <int G, int PB>
-bool cluster_fits(int C) {
-  static int known[kMaxClusterSplits + 1] = {};   // 0 unknown, 1 yes, -1 no
-  if (C < 1 || C > kMaxClusterSplits) return false;
-  int k = __atomic_load_n(&known[C], __ATOMIC_ACQUIRE);
-  if (k != 0) return k > 0;
+int cluster_capacity(int C) {
+  static int known[kMaxClusterSplits + 1] = {};   // 0 unknown, else capacity + 1
+  if (C < 1 || C > kMaxClusterSplits) return 0;
+  const int k = __atomic_load_n(&known[C], __ATOMIC_ACQUIRE);
+  if (k != 0) return k - 1;
   constexpr int STAGES = 3;
   auto kern = decode_kernel<G, STAGES, true, PB>;
   const size_t smem = decode_smem_bytes<G>(STAGES);
@@ -486,6 +487,7 @@ bool cluster_fits(int C) {
                 cudaSuccess &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                 cudaSuccess;
+  int n_clusters = 0;
   if (ok) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(C, 1);
@@ -498,12 +500,14 @@ bool cluster_fits(int C) {
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    int n_clusters = 0;
-    ok = cudaOccupancyMaxActiveClusters(&n_clusters, kern, &lc) == cudaSuccess && n_clusters > 0;
+    ok = cudaOccupancyMaxActiveClusters(&n_clusters, kern, &lc) == cudaSuccess;
   }
-  if (!ok) cudaGetLastError();   // a refused query leaves no error behind
-  __atomic_store_n(&known[C], ok ? 1 : -1, __ATOMIC_RELEASE);
-  return ok;
+  if (!ok) {
+    cudaGetLastError();            // a refused query leaves no error behind
+    n_clusters = 0;
+  }
+  __atomic_store_n(&known[C], n_clusters + 1, __ATOMIC_RELEASE);
+  return n_clusters;
 }
 
 template <int G, int PB>
@@ -542,7 +546,11 @@ int launch_list(DecodeParams p, const CUtensorMap& tk, const CUtensorMap& tv, in
     int pps = std::max(p.pages_per_split, (p.k + kMaxClusterSplits - 1) / kMaxClusterSplits);
     pps = (pps + PPS - 1) / PPS * PPS;
     const int C = (p.k + pps - 1) / pps;
-    if (cluster_fits<G, PB>(C)) {
+    // Only small clusters (at most kMaxMergeCluster CTAs, two SMs): in a decode
+    // step, which starts while the selection's kernels still hold SMs, larger
+    // clusters were measured to start late (32 units in clusters of 8: 5 us
+    // slower per step than the ticketed merge of the same 8 splits).
+    if (C <= kMaxMergeCluster && cluster_capacity<G, PB>(C) > 0) {
       p.pages_per_split = pps;
       return launch_g<G, PB>(p, tk, tv, C, gy, true, stream);
     }

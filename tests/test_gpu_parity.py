@@ -44,7 +44,10 @@ CASES = {
     "b16_slices2": TINY.with_(page_size=16, context=16 * 2500 + 5, global_rank=16,
                               carrier_count=None, carrier_frac=0.01, seed=2023),
     "b16_k40": TINY.with_(page_size=16, budget_tokens=16 * 40, seed=2025),
-    # Llama layer shape at B = 16: k = 128 (radix top-k, 16-split decode clusters)
+    # 80 units: three splits per unit, merged through a thread-block cluster
+    "cluster_merge": TINY.with_(batch=40, context=64 * 20 + 5, seed=2030),
+    "b16_cluster_merge": TINY.with_(page_size=16, batch=40, context=16 * 40 + 3, seed=2031),
+    # Llama layer shape at B = 16: k = 128 (radix top-k)
     "b16_gqa4_k128": TINY.with_(page_size=16, batch=2, n_q_heads=32, n_kv_heads=8,
                                 context=16384, budget_tokens=2048, global_rank=16,
                                 carrier_count=None, carrier_frac=0.01, seed=2024),
