@@ -34,6 +34,13 @@ notes):
   R6  scale 1/sqrt(d); one query per (sequence, query head); the cache holds
       every token including the current one.
   R7  a sequence of length 0 attends nothing: output 0, lse -inf.
+  R8  quantised summary (the deployed form: int4 basis, int8 coefficients and
+      centroid, "per-column and per-row scales"): one scale per basis column,
+      one for the centroid, one per coefficient row; symmetric absmax scales,
+      scale = absmax / qmax (qmax 7 for int4, 127 for int8), code =
+      round-half-even(x / scale) clamped to [-qmax, qmax], all in float32 --
+      the quantiser's own precision, so an integer code is decided in the same
+      precision on both sides; an all-zero group has scale 0 and codes 0.
 """
 from __future__ import annotations
 
@@ -93,6 +100,67 @@ def page_summary(keys: np.ndarray, r: int) -> PageSummary:
         kept += 1
     tail = np.clip(w[r:], 0.0, None).sum() if Bt > r else 0.0
     return PageSummary(mu=mu, V=V, C=C, sigma2=w, tau=float(tail), kept=kept)
+
+
+# --------------------------------------------------------------------------
+# Quantised summary (section 4 "Build": int4 basis, int8 coefficients and
+# centroid, per-column and per-row scales; reading R8)
+# --------------------------------------------------------------------------
+INT4_QMAX = 7
+INT8_QMAX = 127
+
+
+def quantize_symmetric(x, qmax: int) -> Tuple[np.ndarray, np.float32]:
+    """Codes and scale of one group: scale = absmax / qmax, code = x / scale
+    rounded half to even, clamped to [-qmax, qmax]; float32 throughout."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
+    if amax == 0.0:
+        return np.zeros(x.shape, dtype=np.int32), np.float32(0.0)
+    scale = np.float32(amax / np.float32(qmax))
+    codes = np.rint(x / scale)
+    return np.clip(codes, -qmax, qmax).astype(np.int32), scale
+
+
+def dequantize(codes, scale) -> np.ndarray:
+    return np.asarray(codes, dtype=np.float64) * float(scale)
+
+
+@dataclass
+class QuantizedSummary:
+    mu_codes: np.ndarray      # (d,)   int8 codes of the centroid
+    mu_scale: np.float32
+    v_codes: np.ndarray       # (d, r) int4 codes, one scale per column
+    v_scales: np.ndarray      # (r,)
+    c_codes: np.ndarray       # (B, r) int8 codes, one scale per row (token)
+    c_scales: np.ndarray      # (B,)
+
+
+def quantize_summary(mu, V, C) -> QuantizedSummary:
+    """The deployed record of one page summary (mu, V, C given in the values
+    the quantiser reads; float32 rounding is part of the quantiser)."""
+    V = np.asarray(V)
+    C = np.asarray(C)
+    mu_codes, mu_scale = quantize_symmetric(mu, INT8_QMAX)
+    r = V.shape[1]
+    v_codes = np.zeros(V.shape, dtype=np.int32)
+    v_scales = np.zeros(r, dtype=np.float32)
+    for k in range(r):                               # per column
+        v_codes[:, k], v_scales[k] = quantize_symmetric(V[:, k], INT4_QMAX)
+    c_codes = np.zeros(C.shape, dtype=np.int32)
+    c_scales = np.zeros(C.shape[0], dtype=np.float32)
+    for i in range(C.shape[0]):                      # per row
+        c_codes[i], c_scales[i] = quantize_symmetric(C[i], INT8_QMAX)
+    return QuantizedSummary(mu_codes, mu_scale, v_codes, v_scales, c_codes, c_scales)
+
+
+def dequantized_summary(qs: QuantizedSummary) -> PageSummary:
+    """The page summary a quantised record stands for (what the scorer reads)."""
+    mu = dequantize(qs.mu_codes, qs.mu_scale)
+    V = qs.v_codes.astype(np.float64) * qs.v_scales.astype(np.float64)[None, :]
+    C = qs.c_codes.astype(np.float64) * qs.c_scales.astype(np.float64)[:, None]
+    sig = (C ** 2).sum(axis=0)
+    return PageSummary(mu=mu, V=V, C=C, sigma2=sig, tau=0.0, kept=int((sig > 0).sum()))
 
 
 # --------------------------------------------------------------------------

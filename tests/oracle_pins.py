@@ -360,11 +360,74 @@ def pin_paged_attention(O):
         assert np.all(np.isfinite(o))
 
 
+
+
+def pin_quantizer_example(O):
+    """Quantised summary (section 4 "Build", reading R8): hand-computed int4
+    and int8 codes, exact in float32, whose ties fix round-half-even."""
+    fx = _golden("quantizer_example.json")
+    for key in ("int4", "int8"):
+        e = fx[key]
+        codes, scale = O.quantize_symmetric(np.array(e["x"], dtype=np.float32), e["qmax"])
+        assert float(scale) == e["scale"], (key, scale)
+        assert codes.tolist() == e["codes"], (key, codes.tolist())
+    assert O.INT4_QMAX == 7 and O.INT8_QMAX == 127
+
+
+def pin_quantizer_bounds(O):
+    """Symmetric absmax quantisation: |x - code * scale| <= scale / 2, the
+    largest |x| maps to +-qmax, codes stay in [-qmax, qmax], an all-zero group
+    has scale 0 and zero codes, and scaling a group by a power of two scales
+    only its scale."""
+    rng = _rng(23)
+    for qmax in (7, 127):
+        for _ in range(200):
+            x = (rng.standard_normal(int(rng.integers(1, 130))) * rng.uniform(1e-3, 10)).astype(np.float32)
+            codes, scale = O.quantize_symmetric(x, qmax)
+            assert np.abs(codes).max() == qmax
+            assert codes.min() >= -qmax and codes.max() <= qmax
+            err = np.abs(x.astype(np.float64) - codes * float(scale)).max()
+            assert err <= float(scale) * (0.5 + 1e-5), (err, scale)
+            c2, s2 = O.quantize_symmetric(np.float32(4.0) * x, qmax)
+            assert np.array_equal(c2, codes) and float(s2) == 4.0 * float(scale)
+        z, zs = O.quantize_symmetric(np.zeros(9, dtype=np.float32), qmax)
+        assert float(zs) == 0.0 and not z.any()
+
+
+def pin_quantized_summary_groups(O):
+    """Section 4 "Build": one scale per basis column (int4), one per
+    coefficient row and one for the centroid (int8).  Scaling one column of V
+    or one row of C by 2 changes that group's scale only; the dequantised
+    record reconstructs the summary to within half a step per entry."""
+    rng = _rng(29)
+    keys = rng.standard_normal((16, 32))
+    s = O.page_summary(keys, 6)
+    mu, V, C = s.mu.astype(np.float32), s.V.astype(np.float32), s.C.astype(np.float32)
+    q = O.quantize_summary(mu, V, C)
+    assert q.v_codes.shape == V.shape and q.v_scales.shape == (V.shape[1],)
+    assert q.c_codes.shape == C.shape and q.c_scales.shape == (C.shape[0],)
+    assert np.abs(q.v_codes).max() <= 7 and np.abs(q.c_codes).max() <= 127
+    V2 = V.copy(); V2[:, 2] *= 2
+    q2 = O.quantize_summary(mu, V2, C)
+    assert np.array_equal(q2.v_codes, q.v_codes)
+    assert q2.v_scales[2] == 2 * q.v_scales[2]
+    assert np.array_equal(np.delete(q2.v_scales, 2), np.delete(q.v_scales, 2))
+    C2 = C.copy(); C2[5] *= 2
+    q3 = O.quantize_summary(mu, V, C2)
+    assert np.array_equal(q3.c_codes, q.c_codes) and q3.c_scales[5] == 2 * q.c_scales[5]
+    assert np.array_equal(np.delete(q3.c_scales, 5), np.delete(q.c_scales, 5))
+    d = O.dequantized_summary(q)
+    assert np.all(np.abs(d.V - V) <= q.v_scales[None, :] * 0.5 + 1e-7)
+    assert np.all(np.abs(d.C - C) <= q.c_scales[:, None] * 0.5 + 1e-6)
+    assert np.all(np.abs(d.mu - mu) <= float(q.mu_scale) * 0.5 + 1e-7)
+
+
 ALL_PINS = [
     pin_worked_example, pin_isotropic_null, pin_exact_rank, pin_full_rank_r15,
     pin_svd_route, pin_centroid_closed_form, pin_prop2, pin_lemma3,
     pin_shares_and_sandwich, pin_budget_rule, pin_forced_pages, pin_select_bruteforce,
     pin_exact_rank_selection_and_retention, pin_attention, pin_paged_attention,
+    pin_quantizer_example, pin_quantizer_bounds, pin_quantized_summary_groups,
 ]
 # the cheap ones, for the planted-mistake runs
 FAST_PINS = [p for p in ALL_PINS if p is not pin_isotropic_null]

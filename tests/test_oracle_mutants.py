@@ -34,6 +34,14 @@ MUTANTS = {
     "sink_not_forced": ("forced = sorted({0, n - 1})", "forced = sorted({n - 1})"),
     "attend_no_scale": ("logits = q @ K.T / math.sqrt(q.shape[1])", "logits = q @ K.T"),
     "tail_page_all_tokens": ("return max(0, min(page_size, seq_len - j * page_size))", "return page_size"),
+    "quant_round_half_up": ("codes = np.rint(x / scale)", "codes = np.floor(x / scale + 0.5)"),
+    "quant_scale_no_qmax": ("scale = np.float32(amax / np.float32(qmax))",
+                            "scale = np.float32(amax / np.float32(qmax + 1))"),
+    "quant_basis_one_scale": ("v_codes[:, k], v_scales[k] = quantize_symmetric(V[:, k], INT4_QMAX)",
+                              "v_codes[:, k], v_scales[k] = (quantize_symmetric(V, INT4_QMAX)[0][:, k], "
+                              "quantize_symmetric(V, INT4_QMAX)[1])"),
+    "quant_basis_int8": ("v_codes[:, k], v_scales[k] = quantize_symmetric(V[:, k], INT4_QMAX)",
+                         "v_codes[:, k], v_scales[k] = quantize_symmetric(V[:, k], INT8_QMAX)"),
 }
 
 
