@@ -41,7 +41,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("locks", "reference"), default="locks")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
-    ap.add_argument("--summary", choices=("f32", "bf16"), default="f32")
+    ap.add_argument("--summary", choices=("f32", "bf16", "i4"), default="f32",
+                    help="summary record: fp32, bf16, or quantised (int4 basis, int8 "
+                         "coefficients and centroid)")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -323,7 +325,8 @@ def run_gpu(args):
     t0 = time.time()
     inputs = W.generate(w)
     gen_s = time.time() - t0
-    sdt = Bd.LOCKS_SUMMARY_F32 if args.summary == "f32" else Bd.LOCKS_SUMMARY_BF16
+    sdt = {"f32": Bd.LOCKS_SUMMARY_F32, "bf16": Bd.LOCKS_SUMMARY_BF16,
+           "i4": Bd.LOCKS_SUMMARY_I4}[args.summary]
     layer = runtime.LocksLayer.from_inputs(inputs, summary_dtype=sdt)
     stream = torch.cuda.current_stream()
 
@@ -491,7 +494,8 @@ def run_gpu(args):
     peak, peak_kind = measured_peaks()
     sel_mean = sum(sel_ms) / len(sel_ms)
     achieved = select_bytes / (sel_mean / 1e3) / 1e9
-    traffic, prof = profile_traffic("select", w.name if args.summary == "f32" else w.name + "_bf16")
+    traffic, prof = profile_traffic("select", w.name if args.summary == "f32"
+                                    else f"{w.name}_{args.summary}")
     step_gbs = (select_bytes + decode_bytes) / (mean_step / 1e3) / 1e9
     line = {
         "metric": METRIC,

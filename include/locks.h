@@ -70,6 +70,7 @@ extern "C" {
 /* summary record element type */
 #define LOCKS_SUMMARY_F32  0
 #define LOCKS_SUMMARY_BF16 1
+#define LOCKS_SUMMARY_I4   2   /* int4 basis, int8 coefficients and centroid */
 
 typedef struct locks_cfg {
   int32_t batch;          /* sequences in the decode batch (>= 0)                     */
@@ -80,7 +81,7 @@ typedef struct locks_cfg {
   int32_t rank;           /* r, modes kept per page summary                            */
   int32_t max_pages;      /* row stride of block_table (pages per sequence, at most)  */
   int32_t num_blocks;     /* physical blocks in the KV / summary pools                 */
-  int32_t summary_dtype;  /* LOCKS_SUMMARY_F32 or LOCKS_SUMMARY_BF16                   */
+  int32_t summary_dtype;  /* LOCKS_SUMMARY_F32, LOCKS_SUMMARY_BF16 or LOCKS_SUMMARY_I4  */
 } locks_cfg_t;
 
 /*
@@ -97,6 +98,28 @@ typedef struct locks_cfg {
  * (blk * n_kv_heads + h) * locks_summary_record_bytes(cfg) of the pool.  The
  * basis is orthonormal (v_k^T v_l = delta_kl up to rounding), modes are in
  * descending eigenvalue order, and c_i = V^T (k_i - mu) (section 4, "Build").
+ *
+ * LOCKS_SUMMARY_I4 is the quantised record the paper deploys (section 4
+ * "Build": the basis in int4, the coefficients and centroid in int8, with
+ * per-column and per-row scales).  Each group is quantised symmetrically:
+ * scale = max|x| / qmax (qmax 7 for int4, 127 for int8), code =
+ * round-half-even(x / scale) clamped to [-qmax, qmax], in float32; an
+ * all-zero group has scale 0.  Codes are stored biased (int4 + 8 as an
+ * unsigned nibble, int8 + 128 as an unsigned byte).  With HDR = (R + 1) * 4
+ * rounded up to 16 bytes:
+ *
+ *   float    vscale[R], mscale;      scale of basis column k; of the centroid
+ *   uint32_t vq[R][16]         @HDR  word (k, l), byte m (m < 4): low nibble
+ *                                    = code of v_k[4l + m], high nibble = code
+ *                                    of v_k[64 + 4l + m]
+ *   uint8_t  mq[16][2][4]      @HDR + 64R   [l][0][m] = code of mu[4l + m],
+ *                                    [l][1][m] = code of mu[64 + 4l + m]
+ *   uint8_t  cq[B][R]          @HDR + 64R + 128   code of c_{i,k}
+ *   float    cscale[B]         @HDR + 64R + 128 + B R   scale of row c_i
+ *
+ * so that v_k[t] = vscale[k] * (nibble - 8), mu[t] = mscale * (byte - 128),
+ * c_{i,k} = cscale[i] * (byte - 128).  The quantised values are those of the
+ * float record's basis, coefficients and centroid.
  */
 size_t locks_summary_record_bytes(const locks_cfg_t* cfg);
 

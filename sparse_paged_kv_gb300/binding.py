@@ -32,6 +32,7 @@ LOCKS_DEV_BAD_SEQ_LEN = 0x10
 
 LOCKS_SUMMARY_F32 = 0
 LOCKS_SUMMARY_BF16 = 1
+LOCKS_SUMMARY_I4 = 2
 
 
 class LocksLibraryMissing(RuntimeError):
@@ -232,14 +233,51 @@ def locks_dense_decode(cfg: LocksConfig, q, k_cache, v_cache, block_table, seq_l
 # --------------------------------------------------------------------------
 # host-side view of the summary record layout (see locks.h)
 # --------------------------------------------------------------------------
+def unpack_i4(raw, cfg: LocksConfig) -> Tuple:
+    """Codes (unbiased int32) and scales of quantised records [..., record_bytes]
+    (layout in locks.h): mu_codes [..., d], mu_scale [...], v_codes [..., d, R],
+    v_scales [..., R], c_codes [..., B, R], c_scales [..., B]."""
+    import numpy as np
+    d, B, R = cfg.head_dim, cfg.page_size, cfg.rank_cap
+    raw = np.asarray(raw, dtype=np.uint8)
+    lead = raw.shape[:-1]
+    hdr = ((R + 1) * 4 + 15) // 16 * 16
+    off_mq = hdr + 64 * R
+    off_cq = off_mq + 128
+    off_cs = off_cq + B * R
+
+    def f32(a, b):
+        return np.ascontiguousarray(raw[..., a:b]).view(np.float32)
+
+    head = f32(0, 4 * (R + 1))
+    v_scales, mu_scale = head[..., :R], head[..., R]
+    vb = raw[..., hdr:off_mq].reshape(*lead, R, 16, 4).astype(np.int32)   # [k][l][m]
+    lo = (vb & 15).reshape(*lead, R, 64) - 8        # v_k[4l + m]
+    hi = (vb >> 4).reshape(*lead, R, 64) - 8        # v_k[64 + 4l + m]
+    v_codes = np.swapaxes(np.concatenate([lo, hi], axis=-1), -1, -2)
+    mb = raw[..., off_mq:off_cq].reshape(*lead, 16, 2, 4).astype(np.int32)
+    mu_codes = np.concatenate([mb[..., :, 0, :].reshape(*lead, 64),
+                               mb[..., :, 1, :].reshape(*lead, 64)], axis=-1) - 128
+    c_codes = raw[..., off_cq:off_cs].reshape(*lead, B, R).astype(np.int32) - 128
+    c_scales = f32(off_cs, off_cs + 4 * B)
+    return mu_codes, mu_scale, v_codes, v_scales, c_codes, c_scales
+
+
 def unpack_records(raw, cfg: LocksConfig) -> Tuple:
-    """Split host record bytes [..., record_bytes] into (mu, V, C) float64 arrays.
+    """Split host record bytes [..., record_bytes] into (mu, V, C) float64 arrays
+    (a quantised record is dequantised: code times its group's scale).
 
     mu: [..., d]; V: [..., d, rank] (basis columns); C: [..., B, rank]."""
     import numpy as np
     d, B, R = cfg.head_dim, cfg.page_size, cfg.rank_cap
     raw = np.asarray(raw)
     lead = raw.shape[:-1]
+    if cfg.summary_dtype == LOCKS_SUMMARY_I4:
+        mu_c, mu_s, v_c, v_s, c_c, c_s = unpack_i4(raw, cfg)
+        mu = mu_c * mu_s.astype(np.float64)[..., None]
+        V = v_c * v_s.astype(np.float64)[..., None, :]
+        C = c_c * c_s.astype(np.float64)[..., :, None]
+        return mu, V[..., :cfg.rank], C[..., :cfg.rank]
     if cfg.summary_dtype == LOCKS_SUMMARY_F32:
         x = raw.view(np.float32).astype(np.float64)
     else:

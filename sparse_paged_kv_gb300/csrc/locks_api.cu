@@ -25,7 +25,8 @@ int check_cfg(const locks_cfg_t* c) {
       c->num_blocks <= 0 || c->rank <= 0 || c->head_dim <= 0 || c->page_size <= 0)
     return LOCKS_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads != 0) return LOCKS_ERR_INVALID_ARG;
-  if (c->summary_dtype != LOCKS_SUMMARY_F32 && c->summary_dtype != LOCKS_SUMMARY_BF16)
+  if (c->summary_dtype != LOCKS_SUMMARY_F32 && c->summary_dtype != LOCKS_SUMMARY_BF16 &&
+      c->summary_dtype != LOCKS_SUMMARY_I4)
     return LOCKS_ERR_INVALID_ARG;
   if (c->head_dim != kHeadDim || (c->page_size != 64 && c->page_size != 16))
     return LOCKS_ERR_UNSUPPORTED;
@@ -142,6 +143,7 @@ extern "C" {
 size_t locks_summary_record_bytes(const locks_cfg_t* cfg) {
   if (check_cfg(cfg) != LOCKS_OK) return 0;
   const int rp = locks::rank_cap(cfg->rank);
+  if (cfg->summary_dtype == LOCKS_SUMMARY_I4) return size_t(locks::i4_bytes(rp, cfg->page_size));
   return size_t(locks::rec_elems(rp, cfg->page_size)) * elem_bytes(cfg);
 }
 
@@ -152,7 +154,8 @@ size_t locks_select_workspace_bytes(const locks_cfg_t* cfg, int32_t budget_token
   const int k = page_budget(budget_tokens, cfg->page_size);
   if (budget_tokens <= 0 || k < 2) return 0;
   if (cfg->batch == 0) return 0;
-  return locks::select_geometry(cfg->batch * cfg->n_kv_heads, cfg->max_pages, group_of(cfg), k)
+  return locks::select_geometry(cfg->batch * cfg->n_kv_heads, cfg->max_pages, group_of(cfg), k,
+                                locks::score_ctas_per_sm(cfg->summary_dtype))
       .total;
 }
 
@@ -198,7 +201,8 @@ int locks_select(const locks_cfg_t* cfg, const void* q, const void* summaries,
   if (!q || !summaries || !block_table || !seq_lens || !selected || !workspace)
     return LOCKS_ERR_INVALID_ARG;
   const int U = cfg->batch * cfg->n_kv_heads;
-  const locks::SelectGeom L = locks::select_geometry(U, cfg->max_pages, group_of(cfg), k);
+  const locks::SelectGeom L = locks::select_geometry(U, cfg->max_pages, group_of(cfg), k,
+                                                     locks::score_ctas_per_sm(cfg->summary_dtype));
   if (workspace_bytes < L.total) return LOCKS_ERR_WORKSPACE;
   locks::SelectParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);

@@ -15,6 +15,8 @@
 //      coefficients); V = D^T U_r S_r^-1, C = U_r S_r,
 //      tau = sum of the remaining eigenvalues;
 //   5. the record (mu, V, C) in the layout locks_select reads.
+#include <type_traits>
+
 #include "locks_common.cuh"
 #include "locks_internal.h"
 
@@ -39,6 +41,7 @@ struct BuildSmem {
   float red[kBuildThreads / 32 * 2];
   float lam[16];
   int order[16];
+  float qscale[17];             // quantised record: column scales, then the centroid's
   float tau;
   int flag;
 };
@@ -52,6 +55,113 @@ __device__ __forceinline__ void round_pair(int t, int k, int& p, int& q) {
   else { a = (t + k) % (PB - 1); b = (t - k + (PB - 1)) % (PB - 1); }
   p = min(a, b);
   q = max(a, b);
+}
+
+// Quantised record (section 4 "Build": int4 basis with one scale per column,
+// int8 coefficients and centroid with one scale per row): the float values
+// the float record would hold, quantised symmetrically (scale = max|x| /
+// qmax, code = round-half-even(x / scale), IEEE division, clamped), codes
+// stored biased as in the layout of locks.h.
+__device__ __forceinline__ uint32_t quant_biased(float x, float scale, int qmax) {
+  if (!(scale > 0.f)) return uint32_t(qmax + 1);           // code 0
+  const float c = fminf(fmaxf(rintf(__fdiv_rn(x, scale)), float(-qmax)), float(qmax));
+  return uint32_t(int(c) + qmax + 1);
+}
+
+template <int RP, int PB, typename Smem>
+__device__ __forceinline__ void write_i4_record(Smem& S, const BuildParams& prm, int blk, int h,
+                                                int r) {
+  constexpr int kAS = Smem::AS;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned char* rb = static_cast<unsigned char*>(prm.summaries) +
+                      (size_t(blk) * prm.n_kv_heads + h) * prm.rec_bytes;
+  // basis values v_k[t] (as the float record stores them) into the idle D array
+  float v[RP];
+  if (tid < kHeadDim) {
+#pragma unroll
+    for (int k = 0; k < RP; ++k) v[k] = 0.f;
+    for (int i = 0; i < PB; ++i) {
+      const float dit = S.D[i * kDS + tid];
+#pragma unroll
+      for (int k = 0; k < RP; ++k)
+        if (k < r) v[k] += dit * S.U[i * kAS + S.order[k]];
+    }
+  }
+  __syncthreads();
+  float* Vs = S.D;                                         // [RP][d]
+  if (tid < kHeadDim) {
+#pragma unroll
+    for (int k = 0; k < RP; ++k) {
+      const float lam = k < r ? S.lam[k] : 0.f;
+      Vs[k * kHeadDim + tid] = lam > 0.f ? v[k] * rsqrtf(lam) : 0.f;
+    }
+  }
+  __syncthreads();
+  // scales: basis column k (warp k % 8), the centroid (warp 0)
+  for (int k = warp; k < RP; k += kBuildThreads / 32) {
+    float am = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) am = fmaxf(am, fabsf(Vs[k * kHeadDim + lane + 32 * j]));
+    am = group_max<32>(am);
+    if (lane == 0) S.qscale[k] = am > 0.f ? __fdiv_rn(am, 7.f) : 0.f;
+  }
+  if (warp == 0) {
+    float am = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) am = fmaxf(am, fabsf(S.mu[lane + 32 * j]));
+    am = group_max<32>(am);
+    if (lane == 0) S.qscale[16] = am > 0.f ? __fdiv_rn(am, 127.f) : 0.f;
+  }
+  __syncthreads();
+  if (tid < RP * 16) {
+    // basis word (k, l): byte m = code(v_k[4l+m]) | code(v_k[64+4l+m]) << 4
+    const int k = tid >> 4, l = tid & 15;
+    const float sc = S.qscale[k];
+    uint32_t w = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t lo = quant_biased(Vs[k * kHeadDim + 4 * l + m], sc, 7);
+      const uint32_t hi = quant_biased(Vs[k * kHeadDim + 64 + 4 * l + m], sc, 7);
+      w |= (lo | (hi << 4)) << (8 * m);
+    }
+    reinterpret_cast<uint32_t*>(rb + i4_vq(RP))[k * 16 + l] = w;
+  }
+  if (tid < RP) reinterpret_cast<float*>(rb)[tid] = S.qscale[tid];
+  if (tid == RP) reinterpret_cast<float*>(rb)[RP] = S.qscale[16];
+  if (tid >= 224 && tid < 240) {
+    // centroid bytes of lane l
+    const int l = tid - 224;
+    const float sc = S.qscale[16];
+    uint32_t x = 0, y = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      x |= quant_biased(S.mu[4 * l + m], sc, 127) << (8 * m);
+      y |= quant_biased(S.mu[64 + 4 * l + m], sc, 127) << (8 * m);
+    }
+    reinterpret_cast<uint2*>(rb + i4_mq(RP))[l] = make_uint2(x, y);
+  }
+  if (tid >= kBuildThreads - PB) {
+    // coefficient row i: its own scale over the r kept modes
+    const int i = tid - (kBuildThreads - PB);
+    float c[RP];
+    float am = 0.f;
+#pragma unroll
+    for (int k = 0; k < RP; ++k) {
+      const float lam = k < r ? S.lam[k] : 0.f;
+      c[k] = lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
+      am = fmaxf(am, fabsf(c[k]));
+    }
+    const float sc = am > 0.f ? __fdiv_rn(am, 127.f) : 0.f;
+    uint32_t* row = reinterpret_cast<uint32_t*>(rb + i4_cq(RP) + i * RP);
+#pragma unroll
+    for (int k4 = 0; k4 < RP / 4; ++k4) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w |= quant_biased(c[4 * k4 + e], sc, 127) << (8 * e);
+      row[k4] = w;
+    }
+    reinterpret_cast<float*>(rb + i4_cscale(RP, PB))[i] = sc;
+  }
 }
 
 template <int RP, typename T, int PB>
@@ -245,32 +355,36 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   __syncthreads();
 
   // ---- 5. record: W[0] = mu, W[1+k] = v_k, C[c][i][e] = u_ik sigma_k ----------
-  T* rec = reinterpret_cast<T*>(static_cast<unsigned char*>(prm.summaries) +
-                                (size_t(blk) * prm.n_kv_heads + h) * prm.rec_bytes);
-  if (tid < kHeadDim) {
-    const int t = tid;
-    st_elem(rec + t, S.mu[t]);
-    float v[RP];
-#pragma unroll
-    for (int k = 0; k < RP; ++k) v[k] = 0.f;
-    for (int i = 0; i < PB; ++i) {
-      const float dit = S.D[i * kDS + t];
-#pragma unroll
-      for (int k = 0; k < RP; ++k)
-        if (k < r) v[k] += dit * S.U[i * kAS + S.order[k]];
-    }
-#pragma unroll
-    for (int k = 0; k < RP; ++k) {
-      const float lam = k < r ? S.lam[k] : 0.f;
-      st_elem(rec + (1 + k) * kHeadDim + t, lam > 0.f ? v[k] * rsqrtf(lam) : 0.f);
-    }
+  if constexpr (std::is_same_v<T, I4Rec>) {
+    write_i4_record<RP, PB>(S, prm, blk, h, r);
   } else {
-    T* C = rec + rec_w_elems(RP);
-    for (int idx = tid - kHeadDim; idx < PB * RP; idx += kBuildThreads - kHeadDim) {
-      const int i = idx / RP, k = idx % RP;
-      const float lam = k < r ? S.lam[k] : 0.f;
-      const float c = lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
-      st_elem(C + ((k >> 2) * PB + i) * 4 + (k & 3), c);
+    T* rec = reinterpret_cast<T*>(static_cast<unsigned char*>(prm.summaries) +
+                                  (size_t(blk) * prm.n_kv_heads + h) * prm.rec_bytes);
+    if (tid < kHeadDim) {
+      const int t = tid;
+      st_elem(rec + t, S.mu[t]);
+      float v[RP];
+#pragma unroll
+      for (int k = 0; k < RP; ++k) v[k] = 0.f;
+      for (int i = 0; i < PB; ++i) {
+        const float dit = S.D[i * kDS + t];
+#pragma unroll
+        for (int k = 0; k < RP; ++k)
+          if (k < r) v[k] += dit * S.U[i * kAS + S.order[k]];
+      }
+#pragma unroll
+      for (int k = 0; k < RP; ++k) {
+        const float lam = k < r ? S.lam[k] : 0.f;
+        st_elem(rec + (1 + k) * kHeadDim + t, lam > 0.f ? v[k] * rsqrtf(lam) : 0.f);
+      }
+    } else {
+      T* C = rec + rec_w_elems(RP);
+      for (int idx = tid - kHeadDim; idx < PB * RP; idx += kBuildThreads - kHeadDim) {
+        const int i = idx / RP, k = idx % RP;
+        const float lam = k < r ? S.lam[k] : 0.f;
+        const float c = lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
+        st_elem(C + ((k >> 2) * PB + i) * 4 + (k & 3), c);
+      }
     }
   }
   if (tid == 0) {
@@ -290,23 +404,29 @@ int launch_t(const BuildParams& p, cudaStream_t stream) {
   return cudaPeekAtLastError() == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
 }
 
-template <int PB>
-int launch_pb(const BuildParams& p, int RP, bool f32, cudaStream_t stream) {
+template <int PB, typename T>
+int launch_rp(const BuildParams& p, int RP, cudaStream_t stream) {
   switch (RP) {
-    case 4: return f32 ? launch_t<4, float, PB>(p, stream) : launch_t<4, __nv_bfloat16, PB>(p, stream);
-    case 8: return f32 ? launch_t<8, float, PB>(p, stream) : launch_t<8, __nv_bfloat16, PB>(p, stream);
-    case 16:
-      return f32 ? launch_t<16, float, PB>(p, stream) : launch_t<16, __nv_bfloat16, PB>(p, stream);
+    case 4: return launch_t<4, T, PB>(p, stream);
+    case 8: return launch_t<8, T, PB>(p, stream);
+    case 16: return launch_t<16, T, PB>(p, stream);
     default: return LOCKS_ERR_UNSUPPORTED;
   }
+}
+
+template <int PB>
+int launch_pb(const BuildParams& p, int RP, int dtype, cudaStream_t stream) {
+  if (dtype == LOCKS_SUMMARY_F32) return launch_rp<PB, float>(p, RP, stream);
+  if (dtype == LOCKS_SUMMARY_BF16) return launch_rp<PB, __nv_bfloat16>(p, RP, stream);
+  if (dtype == LOCKS_SUMMARY_I4) return launch_rp<PB, I4Rec>(p, RP, stream);
+  return LOCKS_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
 int launch_build(const BuildParams& p, int RP, int dtype, int page_size, cudaStream_t stream) {
-  const bool f32 = dtype == LOCKS_SUMMARY_F32;
-  if (page_size == 64) return launch_pb<64>(p, RP, f32, stream);
-  if (page_size == 16) return launch_pb<16>(p, RP, f32, stream);
+  if (page_size == 64) return launch_pb<64>(p, RP, dtype, stream);
+  if (page_size == 16) return launch_pb<16>(p, RP, dtype, stream);
   return LOCKS_ERR_UNSUPPORTED;
 }
 

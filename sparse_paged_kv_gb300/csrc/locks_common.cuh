@@ -28,6 +28,17 @@ __host__ __device__ constexpr int rank_cap(int r) { return r <= 4 ? 4 : (r <= 8 
 __host__ __device__ constexpr int rec_w_elems(int rp) { return (rp + 1) * kHeadDim; }
 __host__ __device__ constexpr int rec_elems(int rp, int B) { return (rp + 1) * kHeadDim + rp * B; }
 
+// Quantised record (LOCKS_SUMMARY_I4) byte offsets; see the layout in locks.h.
+__host__ __device__ constexpr int i4_hdr(int rp) { return ((rp + 1) * 4 + 15) / 16 * 16; }
+__host__ __device__ constexpr int i4_vq(int rp) { return i4_hdr(rp); }
+__host__ __device__ constexpr int i4_mq(int rp) { return i4_hdr(rp) + 64 * rp; }
+__host__ __device__ constexpr int i4_cq(int rp) { return i4_mq(rp) + 128; }
+__host__ __device__ constexpr int i4_cscale(int rp, int B) { return i4_cq(rp) + B * rp; }
+__host__ __device__ constexpr int i4_bytes(int rp, int B) { return i4_cscale(rp, B) + 4 * B; }
+
+// Tag type of the quantised record in the kernels' templates.
+struct I4Rec {};
+
 // ---------------------------------------------------------------------------
 // status words
 // ---------------------------------------------------------------------------

@@ -8,6 +8,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/locks.h"
+
 namespace locks {
 
 constexpr size_t kMaxDynSmem = 227 * 1024;
@@ -79,7 +81,11 @@ struct BuildParams {
   int n_blocks, n_kv_heads, num_blocks, rank, max_sweeps;
 };
 
-SelectGeom select_geometry(int units, int max_pages, int G, int k);
+// ctas_per_sm: score CTAs per SM the grid is sized for (see score_ctas_per_sm)
+SelectGeom select_geometry(int units, int max_pages, int G, int k, int ctas_per_sm);
+// Score CTAs per SM for a summary type: 4 for the quantised record (small
+// records, denser arithmetic: more warps to hide instruction latency), else 2.
+inline int score_ctas_per_sm(int summary_dtype) { return summary_dtype == LOCKS_SUMMARY_I4 ? 4 : 2; }
 // score kernel only, one definition per page size (locks_select.cu: 64,
 // locks_score_b16.cu: 16)
 int launch_score_b64(const SelectParams& p, int G, int RP, int dtype, int n_ctas,

@@ -4,6 +4,8 @@
 // by one translation unit per page size; internal to the library.
 #pragma once
 
+#include <type_traits>
+
 #include "locks_common.cuh"
 #include "locks_internal.h"
 
@@ -44,6 +46,17 @@ __device__ __forceinline__ float dot8(const float4& qa, const float4& qb, const 
   return acc.x + acc.y;
 }
 
+// Four biased codes (the bytes of w) as floats minus their bias: each byte is
+// placed in the mantissa of 2^23 (exact) and 2^23 + bias is subtracted.
+__device__ __forceinline__ float4 biased_bytes_f4(uint32_t w, float bias_plus_2p23) {
+  return make_float4(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7540)) - bias_plus_2p23,
+                     __int_as_float(__byte_perm(w, 0x4B000000u, 0x7541)) - bias_plus_2p23,
+                     __int_as_float(__byte_perm(w, 0x4B000000u, 0x7542)) - bias_plus_2p23,
+                     __int_as_float(__byte_perm(w, 0x4B000000u, 0x7543)) - bias_plus_2p23);
+}
+constexpr float kI4Off = 8388616.f;     // 2^23 + 8   (int4 codes stored + 8)
+constexpr float kI8Off = 8388736.f;     // 2^23 + 128 (int8 codes stored + 128)
+
 // Scores one page summary `rec` in each half-warp (lane hl = lane % 16 of the
 // half).  Returns s_hat of head hl / (16/G) (identical across that head's lanes).
 template <int G, int RP, typename T, int PB>
@@ -56,32 +69,56 @@ __device__ __forceinline__ float score_page16(const T* __restrict__ rec, const f
   constexpr int LG = kHalf / G;                // lanes per head after the G-value reductions
   const int lane = threadIdx.x & 31;
 
+  constexpr bool kI4 = std::is_same_v<T, I4Rec>;
+  const unsigned char* rb = reinterpret_cast<const unsigned char*>(rec);
   float pv[NP];
   float av[G];
-  {
-    const float4 wa = ld4(rec + 4 * hl), wb = ld4(rec + 64 + 4 * hl);   // centroid
+  if constexpr (kI4) {
+    // quantised record: codes -> floats, dot, then the group scales after the
+    // reductions (a = mscale * q.codes(mu), p_k = vscale[k] * q.codes(v_k))
+    const uint2 mw = reinterpret_cast<const uint2*>(rb + i4_mq(RP))[hl];
+    const float4 wa = biased_bytes_f4(mw.x, kI8Off), wb = biased_bytes_f4(mw.y, kI8Off);
 #pragma unroll
     for (int g = 0; g < G; ++g) av[g] = dot8(qa[g], qb[g], wa, wb);
-  }
+    const uint32_t* vq = reinterpret_cast<const uint32_t*>(rb + i4_vq(RP));
 #pragma unroll
-  for (int k = 0; k < RP; ++k) {
-    const float4 wa = ld4(rec + (1 + k) * kHeadDim + 4 * hl);
-    const float4 wb = ld4(rec + (1 + k) * kHeadDim + 64 + 4 * hl);
+    for (int k = 0; k < RP; ++k) {
+      const uint32_t w = vq[k * 16 + hl];
+      const float4 va = biased_bytes_f4(w & 0x0F0F0F0Fu, kI4Off);
+      const float4 vb = biased_bytes_f4((w >> 4) & 0x0F0F0F0Fu, kI4Off);
 #pragma unroll
-    for (int g = 0; g < G; ++g) pv[g * RP + k] = dot8(qa[g], qb[g], wa, wb);
+      for (int g = 0; g < G; ++g) pv[g * RP + k] = dot8(qa[g], qb[g], va, vb);
+    }
+  } else {
+    {
+      const float4 wa = ld4(rec + 4 * hl), wb = ld4(rec + 64 + 4 * hl);   // centroid
+#pragma unroll
+      for (int g = 0; g < G; ++g) av[g] = dot8(qa[g], qb[g], wa, wb);
+    }
+#pragma unroll
+    for (int k = 0; k < RP; ++k) {
+      const float4 wa = ld4(rec + (1 + k) * kHeadDim + 4 * hl);
+      const float4 wb = ld4(rec + (1 + k) * kHeadDim + 64 + 4 * hl);
+#pragma unroll
+      for (int g = 0; g < G; ++g) pv[g * RP + k] = dot8(qa[g], qb[g], wa, wb);
+    }
   }
   TransposeReduce<NP, kHalf / 2>::run(pv, lane);
   TransposeReduce<G, kHalf / 2>::run(av, lane);
   // lane hl holds p values [(hl / (16/SP)) * VP, +VP) and a of head hl / LG
+  if constexpr (kI4) av[0] *= reinterpret_cast<const float*>(rb)[RP];
   if ((hl & (kHalf / SP - 1)) == 0) {
 #pragma unroll
-    for (int e = 0; e < VP; ++e) pbuf[(hl / (kHalf / SP)) * VP + e] = pv[e];
+    for (int e = 0; e < VP; ++e) {
+      const int idx = (hl / (kHalf / SP)) * VP + e;
+      if constexpr (kI4) pbuf[idx] = pv[e] * reinterpret_cast<const float*>(rb)[idx % RP];
+      else pbuf[idx] = pv[e];
+    }
   }
   __syncwarp();
 
   // reconstructed logits (before the 1/sqrt(d) scale) of tokens hl + 16t
   constexpr int TPL = PB / kHalf;              // tokens per lane (4 or 1)
-  const T* C = rec + rec_w_elems(RP);
   float4 pr[G][RP / 4];
 #pragma unroll
   for (int g = 0; g < G; ++g)
@@ -94,17 +131,24 @@ __device__ __forceinline__ float score_page16(const T* __restrict__ rec, const f
     float2 acc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+    const int i = hl + kHalf * t;
 #pragma unroll
     for (int cc = 0; cc < RP / 4; ++cc) {
-      const float4 c = ld4(C + (cc * PB + hl + kHalf * t) * 4);
+      float4 c;
+      if constexpr (kI4)
+        c = biased_bytes_f4(reinterpret_cast<const uint32_t*>(rb + i4_cq(RP) + i * RP)[cc], kI8Off);
+      else
+        c = ld4(rec + rec_w_elems(RP) + (cc * PB + i) * 4);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         acc[g] = ffma2(make_float2(pr[g][cc].x, pr[g][cc].y), make_float2(c.x, c.y), acc[g]);
         acc[g] = ffma2(make_float2(pr[g][cc].z, pr[g][cc].w), make_float2(c.z, c.w), acc[g]);
       }
     }
+    float row = 1.f;                            // the row's scale (quantised record)
+    if constexpr (kI4) row = reinterpret_cast<const float*>(rb + i4_cscale(RP, PB))[i];
 #pragma unroll
-    for (int g = 0; g < G; ++g) x[g][t] = acc[g].x + acc[g].y;
+    for (int g = 0; g < G; ++g) x[g][t] = (acc[g].x + acc[g].y) * row;
   }
   // log-sum-exp per head: transposed max, broadcast, exponentials, transposed sum
   float mx[G];
@@ -285,7 +329,9 @@ __global__ void __launch_bounds__(kSelThreads, (G >= 8 || G * RP >= 64 || sizeof
 
 template <int G, int RP, typename T, int PB>
 int launch_score_t(const SelectParams& p, int n_ctas, cudaStream_t stream) {
-  constexpr int STAGES = 2;
+  // ring depth: enough record bytes in flight per warp to cover the memory
+  // latency (a quantised record is about a fifth of a float one)
+  constexpr int STAGES = std::is_same_v<T, I4Rec> ? 4 : 2;
   const size_t smem = size_t(kSelWarps) * STAGES * 2 * p.rec_bytes +
                       kSelWarps * STAGES * sizeof(uint64_t) +
                       kSelWarps * 2 * pbuf_stride<G, RP>() * sizeof(float) +
@@ -318,6 +364,7 @@ template <int PB>
 int launch_score_pb(const SelectParams& p, int G, int RP, int dtype, int n_ctas,
                     cudaStream_t stream) {
   if (dtype == LOCKS_SUMMARY_F32) return score_dispatch<float, PB>(p, G, RP, n_ctas, stream);
+  if (dtype == LOCKS_SUMMARY_I4) return score_dispatch<I4Rec, PB>(p, G, RP, n_ctas, stream);
   return score_dispatch<__nv_bfloat16, PB>(p, G, RP, n_ctas, stream);
 }
 

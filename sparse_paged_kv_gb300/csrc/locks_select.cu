@@ -324,15 +324,17 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
-SelectGeom select_geometry(int units, int max_pages, int G, int k) {
+SelectGeom select_geometry(int units, int max_pages, int G, int k, int ctas_per_sm) {
   SelectGeom g;
   const int K = k > 2 ? k - 2 : 1;
   g.mc = (max_pages > 2 ? max_pages - 2 : 1);
   g.mc += g.mc & 1;                                   // even: page pairs never straddle units
   const long total = long(units) * g.mc;
-  // about two CTAs per SM on 152 SMs, at least 16 slots each, a CTA spanning
-  // at most kUnitSlots units, and the slot ids of one CTA in shared memory
-  long per = (total + 2 * 152 - 1) / (2 * 152);
+  // about ctas_per_sm CTAs per SM on 152 SMs, at least 16 slots each, a CTA
+  // spanning at most kUnitSlots units, and the slot ids of one CTA in shared
+  // memory
+  const long ctas = long(ctas_per_sm > 0 ? ctas_per_sm : 2) * 152;
+  long per = (total + ctas - 1) / ctas;
   per += per & 1;
   if (per < 16) per = 16;
   if (per > 2048) per = 2048;

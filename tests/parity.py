@@ -259,9 +259,9 @@ def run_case(inputs, units=None, dense=True, check_build=True, summary_dtype=0):
     """Build, select, sparse- and dense-decode on the GPU; compare the given
     units (default: all) with the oracle.  Returns (report, layer, snapshot).
 
-    summary_dtype 1 (bf16 records): the build is measured, not gated
-    (report.max_record_err), and selection/scores are gated against the oracle
-    scoring the GPU-stored records."""
+    summary_dtype 1 (bf16 records) or 2 (quantised records): the build is
+    measured, not gated (report.max_record_err), and selection/scores are
+    gated against the oracle scoring the GPU-stored records."""
     import torch
     from sparse_paged_kv_gb300 import runtime
     w = inputs.workload
@@ -289,11 +289,11 @@ def run_case(inputs, units=None, dense=True, check_build=True, summary_dtype=0):
     if units is None:
         units = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
     for b, h in units:
-        stored = records_as_summaries(layer, inputs, b, h) if summary_dtype == 1 else None
+        stored = records_as_summaries(layer, inputs, b, h) if summary_dtype != 0 else None
         res = O.run_unit(inputs.q, inputs.k_cache, inputs.v_cache, inputs.block_table,
                          inputs.seq_lens, w.n_kv_heads, w.rank, w.budget_tokens, b, h, dense=dense,
                          summaries=stored)
-        if check_build and summary_dtype == 1:
+        if check_build and summary_dtype != 0:
             fp64 = O.build_unit(inputs.k_cache, inputs.block_table, int(inputs.seq_lens[b]), b, h,
                                 w.rank)
             rep.max_record_err = max(rep.max_record_err, record_error(layer, inputs, b, h, fp64))

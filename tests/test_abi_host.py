@@ -141,3 +141,40 @@ def test_unpack_records_layout():
     raw = np.concatenate([W, C4]).view(np.uint8)
     m2, V2, C2 = B.unpack_records(raw[None], c)
     assert np.array_equal(m2[0], mu) and np.array_equal(V2[0], V) and np.array_equal(C2[0], C)
+
+
+def test_unpack_i4_layout(lib):
+    """The quantised record layout documented in locks.h, packed here by hand,
+    unpacks to the codes and scales it was packed from."""
+    import numpy as np
+    c = cfg(summary_dtype=B.LOCKS_SUMMARY_I4, rank=8)
+    R, Bp, d = c.rank_cap, c.page_size, c.head_dim
+    nbytes = B.summary_record_bytes(c)
+    hdr = ((R + 1) * 4 + 15) // 16 * 16
+    assert nbytes == hdr + 64 * R + 128 + Bp * R + 4 * Bp
+    rng = np.random.default_rng(3)
+    v = rng.integers(-7, 8, (d, R))
+    mu = rng.integers(-127, 128, d)
+    cc = rng.integers(-127, 128, (Bp, R))
+    vs = rng.random(R).astype(np.float32)
+    cs = rng.random(Bp).astype(np.float32)
+    rec = np.zeros(nbytes, np.uint8)
+    rec[:4 * R] = vs.view(np.uint8)
+    rec[4 * R:4 * R + 4] = np.float32(0.25).reshape(1).view(np.uint8)
+    for k in range(R):
+        for l in range(16):
+            for m in range(4):
+                rec[hdr + (k * 16 + l) * 4 + m] = (v[4 * l + m, k] + 8) | ((v[64 + 4 * l + m, k] + 8) << 4)
+    for l in range(16):
+        for m in range(4):
+            rec[hdr + 64 * R + l * 8 + m] = mu[4 * l + m] + 128
+            rec[hdr + 64 * R + l * 8 + 4 + m] = mu[64 + 4 * l + m] + 128
+    rec[hdr + 64 * R + 128:hdr + 64 * R + 128 + Bp * R] = (cc + 128).reshape(-1)
+    rec[hdr + 64 * R + 128 + Bp * R:] = cs.view(np.uint8)
+    mu_c, mu_s, v_c, v_s, c_c, c_s = B.unpack_i4(rec[None], c)
+    assert np.array_equal(mu_c[0], mu) and float(mu_s[0]) == 0.25
+    assert np.array_equal(v_c[0], v) and np.array_equal(v_s[0], vs)
+    assert np.array_equal(c_c[0], cc) and np.array_equal(c_s[0], cs)
+    m, V, C = B.unpack_records(rec[None], c)
+    assert np.allclose(V[0], v * vs[None, :]) and np.allclose(C[0], cc * cs[:, None])
+    assert np.allclose(m[0], mu * 0.25)

@@ -67,3 +67,18 @@ def test_full_size_bf16_records():
     torch.cuda.empty_cache()
     print(f"llama32k bf16: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} record vs fp64 "
           f"{rep.max_record_err:.2e} ties {rep.tie_diffs}")
+
+
+def test_full_size_i4_records():
+    """llama32k with quantised records (int4 basis), two sampled units end to end."""
+    import torch
+    w = W.get("llama32k")
+    inputs = W.generate(w)
+    rep, layer, snap = P.run_case(inputs, units=[(0, 0), (w.batch - 1, w.n_kv_heads - 1)],
+                                  dense=False, summary_dtype=2)
+    rep.check()
+    assert snap["status"] == 0
+    del layer
+    torch.cuda.empty_cache()
+    print(f"llama32k i4: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} record vs fp64 "
+          f"{rep.max_record_err:.2e} ties {rep.tie_diffs}")

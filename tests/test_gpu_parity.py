@@ -92,6 +92,57 @@ def test_parity_bf16_records(name):
           f"{rep.max_record_err:.2e} ties {rep.tie_diffs}")
 
 
+I4_CASES = ["tiny", "ragged", "group8", "rank16", "rank3", "multichunk", "slices3", "k40", "b16",
+            "b16_ragged", "cluster_merge"]
+
+
+@pytest.mark.parametrize("name", I4_CASES)
+def test_parity_i4_records(name):
+    """Quantised records (int4 basis, int8 coefficients and centroid):
+    selection and scores against the oracle scoring the stored codes; decode as
+    for fp32; the dequantised record's distance from the fp64 summary reported."""
+    inputs = W.generate(CASES[name])
+    rep, layer, snap = P.run_case(inputs, summary_dtype=2)
+    rep.check()
+    assert rep.units == CASES[name].batch * CASES[name].n_kv_heads
+    # an int4 basis keeps 4 bits: its reconstruction is a coarse copy
+    assert rep.max_record_err < 0.25, rep.max_record_err
+    print(f"i4 {name}: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} record vs fp64 "
+          f"{rep.max_record_err:.2e} ties {rep.tie_diffs}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "rank16", "rank3", "b16"])
+def test_i4_codes_equal_oracle_quantiser(name):
+    """The GPU's quantised record holds exactly the oracle quantiser's codes and
+    scales of the GPU's own float record (same pages, same build): every
+    integer code is decided in float32 on both sides."""
+    import torch
+    from sparse_paged_kv_gb300 import binding as Bd, runtime
+    w = CASES[name]
+    inputs = W.generate(w)
+    lay = {}
+    for dt in (Bd.LOCKS_SUMMARY_F32, Bd.LOCKS_SUMMARY_I4):
+        lay[dt] = runtime.LocksLayer.from_inputs(inputs, summary_dtype=dt)
+        lay[dt].build()
+    torch.cuda.synchronize()
+    r = w.rank
+    for b, h in [(0, 0), (w.batch - 1, w.n_kv_heads - 1)]:
+        _, cand = O.forced_and_candidates(int(inputs.seq_lens[b]), w.page_size)
+        blocks = inputs.block_table[b, [int(j) for j in cand]]
+        mu32, V32, C32 = lay[Bd.LOCKS_SUMMARY_F32].host_records(blocks, h)
+        raw = lay[Bd.LOCKS_SUMMARY_I4].summaries[torch.as_tensor(blocks).long().cuda(), h]
+        mu_c, mu_s, v_c, v_s, c_c, c_s = Bd.unpack_i4(raw.cpu().numpy(), lay[Bd.LOCKS_SUMMARY_I4].cfg)
+        for n in range(len(blocks)):
+            q = O.quantize_summary(mu32[n].astype(np.float32), V32[n].astype(np.float32),
+                                   C32[n].astype(np.float32))
+            assert np.array_equal(q.mu_codes, mu_c[n]) and q.mu_scale == mu_s[n], (b, h, n)
+            assert np.array_equal(q.v_codes, v_c[n][:, :r]), (b, h, n)
+            assert np.array_equal(q.v_scales, v_s[n][:r]), (b, h, n)
+            assert not v_c[n][:, r:].any() and not v_s[n][r:].any()
+            assert np.array_equal(q.c_codes, c_c[n][:, :r]) and not c_c[n][:, r:].any()
+            assert np.array_equal(q.c_scales, c_s[n]), (b, h, n)
+
+
 def test_empty_sequence_outputs_zero():
     inputs = W.generate(CASES["ragged"])
     rep, layer, snap = P.run_case(inputs, units=[(4, 0), (4, 1)])
