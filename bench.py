@@ -169,6 +169,26 @@ def profile_traffic(kernel_key: str, config: str):
 # --------------------------------------------------------------------------
 # replicas across ranks (weak scaling: every rank runs its own batch)
 # --------------------------------------------------------------------------
+def captured_energy(layer, ids_t, tail, w, sample: int = 4096):
+    """Energy the rank-r summary captures per page-head, 1 - tau / ||D||_F^2
+    (a diagnostic the paper reports for real pages, App. D): tau is the build's
+    tail output; ||D||_F^2 of the centred keys is recomputed for a seeded
+    sample of page-heads.  Outside the timed region."""
+    import torch
+    n = ids_t.numel()
+    if n == 0:
+        return None
+    g = torch.Generator(device="cpu").manual_seed(12345)
+    pick = torch.randperm(n, generator=g)[:max(1, sample // w.n_kv_heads)].to(ids_t.device)
+    K = layer.k_cache[ids_t[pick].long()].float()               # [s, H_kv, B, d]
+    D = K - K.mean(dim=2, keepdim=True)
+    trace = (D * D).sum(dim=(2, 3))                              # [s, H_kv]
+    frac = (1.0 - tail[pick] / trace.clamp_min(1e-30)).flatten().cpu()
+    q = torch.quantile(frac, torch.tensor([0.1, 0.5, 0.9]))
+    return {"page_heads_sampled": int(frac.numel()), "median": float(q[1]),
+            "p10": float(q[0]), "p90": float(q[2]), "mean": float(frac.mean())}
+
+
 def replica_workload(w, rank: int):
     """Rank r's replica of workload w: same shapes, its own seed."""
     return w.with_(seed=w.seed + 7919 * rank) if rank else w
@@ -334,7 +354,9 @@ def run_gpu(args):
     ids = runtime.complete_page_blocks(inputs.block_table, inputs.seq_lens, w.page_size)
     ids_t = torch.from_numpy(ids).cuda()
     bstat = torch.zeros((len(ids), w.n_kv_heads), dtype=torch.int32, device="cuda")
-    layer.build(ids_t, status=bstat)
+    tail = torch.zeros((len(ids), w.n_kv_heads), dtype=torch.float32, device="cuda")
+    layer.build(ids_t, status=bstat, tail_energy=tail)
+    captured = captured_energy(layer, ids_t, tail, w)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     build_ms = []
@@ -530,7 +552,8 @@ def run_gpu(args):
         "dense": dense,
         "speedup_vs_dense": (dense["us_per_step"] / (mean_step * 1e3)) if dense else None,
         "build": {"ms": build_ms, "page_heads": page_heads, "pages_per_s": len(ids) / (build_ms / 1e3),
-                  "page_heads_per_s": page_heads / (build_ms / 1e3), "not_converged": not_conv},
+                  "page_heads_per_s": page_heads / (build_ms / 1e3), "not_converged": not_conv,
+                  "captured_energy": captured},
         "e2e": e2e,
         "gpu_launches": 3 * K,
         "clocks": clocks,
