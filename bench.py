@@ -370,6 +370,24 @@ def run_gpu(args):
     page_heads = len(ids) * w.n_kv_heads
     not_conv = int(((bstat.cpu().numpy() >> 16) != 0).sum())
 
+    # In a decode loop each sequence completes a page every B steps and its
+    # summary is built then (off the step's critical path, section 4): time the
+    # build of one page per sequence (its last complete page, every KV head).
+    last = torch.from_numpy(np.array(
+        [inputs.block_table[b, max(0, int(inputs.seq_lens[b]) // w.page_size - 1)]
+         for b in range(w.batch)], dtype=np.int32)).cuda()
+    for _ in range(3):
+        layer.build(last)
+    torch.cuda.synchronize()
+    crossing_us = []
+    for _ in range(20):
+        e0.record(stream)
+        layer.build(last)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        crossing_us.append(e0.elapsed_time(e1) * 1e3)
+    crossing_us = statistics.median(crossing_us)
+
     # L2 flush between steps: write 256 MiB (> the 129 MB L2), then read another
     # 256 MiB so the dirty lines are written back before the next timed step
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
@@ -553,7 +571,12 @@ def run_gpu(args):
         "speedup_vs_dense": (dense["us_per_step"] / (mean_step * 1e3)) if dense else None,
         "build": {"ms": build_ms, "page_heads": page_heads, "pages_per_s": len(ids) / (build_ms / 1e3),
                   "page_heads_per_s": page_heads / (build_ms / 1e3), "not_converged": not_conv,
-                  "captured_energy": captured},
+                  "captured_energy": captured,
+                  "page_crossing_us": crossing_us,
+                  "page_crossing_per_step_us": crossing_us / w.page_size,
+                  "page_crossing_fraction_of_step": crossing_us / w.page_size / (mean_step * 1e3),
+                  "page_crossing_note": "one completed page per sequence (all KV heads) "
+                                        "built every B decode steps; amortised per step"},
         "e2e": e2e,
         "gpu_launches": 3 * K,
         "clocks": clocks,
