@@ -39,7 +39,8 @@
  *    a workspace must not overlap on the GPU.
  *
  * Supported shapes: head_dim = 128; page_size = 64 or 16; 1 <= rank <= 16;
- * G in {1, 2, 4, 8}.  Other values return LOCKS_ERR_UNSUPPORTED.
+ * G in {1, 2, 4, 8}; max_pages < 2^24; num_blocks * n_kv_heads < 2^31.
+ * Other values return LOCKS_ERR_UNSUPPORTED.
  */
 #ifndef LOCKS_H_
 #define LOCKS_H_
@@ -105,19 +106,27 @@ typedef struct locks_cfg {
  * scale = max|x| / qmax (qmax 7 for int4, 127 for int8), code =
  * round-half-even(x / scale) clamped to [-qmax, qmax], in float32; an
  * all-zero group has scale 0.  Codes are stored biased (int4 + 8 as an
- * unsigned nibble, int8 + 128 as an unsigned byte).  With HDR = (R + 1) * 4
- * rounded up to 16 bytes:
+ * unsigned nibble, int8 + 128 as an unsigned byte), in the order the
+ * scorer's tensor-core fragments read them.  With HDR = (R + 1) * 4 rounded
+ * up to 16 bytes, KK = ceil(R / 8), and for a lane l = 4g + t (g < 8, t < 4):
  *
  *   float    vscale[R], mscale;      scale of basis column k; of the centroid
- *   uint32_t vq[R][16]         @HDR  word (k, l), byte m (m < 4): low nibble
- *                                    = code of v_k[4l + m], high nibble = code
- *                                    of v_k[64 + 4l + m]
- *   uint8_t  mq[16][2][4]      @HDR + 64R   [l][0][m] = code of mu[4l + m],
- *                                    [l][1][m] = code of mu[64 + 4l + m]
- *   uint8_t  cq[B][R]          @HDR + 64R + 128   code of c_{i,k}
- *   float    cscale[B]         @HDR + 64R + 128 + B R   scale of row c_i
+ *   uint32_t vq[R][4][4]       @HDR  word vq[k][t][j] holds, for the k-steps
+ *                                    s = 2j and 2j + 1 (columns 16s + c):
+ *                                    nibbles 0 / 4 = v_k at c = 2t / 2t + 1,
+ *                                    nibbles 1 / 5 = c = 2t + 8 / 2t + 9 (k-step
+ *                                    2j), nibbles 2 / 6 and 3 / 7 the same for
+ *                                    k-step 2j + 1
+ *   uint8_t  mq[32][4]         @HDR + 64R   mq[l] = mu at 16g + 2t, 16g + 2t + 1,
+ *                                    16g + 2t + 8, 16g + 2t + 9
+ *   uint8_t  cq[B/16][KK][32][4]  @HDR + 64R + 128   cq[m][kk][l] = c_{i,k} at
+ *                                    (i, k) = (16m + g, 8kk + 2t), (16m + g,
+ *                                    8kk + 2t + 1), (16m + g + 8, 8kk + 2t),
+ *                                    (16m + g + 8, 8kk + 2t + 1)
+ *   float    cscale[B]         @HDR + 64R + 128 + 8 B KK   scale of row c_i
  *
- * so that v_k[t] = vscale[k] * (nibble - 8), mu[t] = mscale * (byte - 128),
+ * (nibble n of a word is bits 4n..4n+3; codes of columns k >= rank are 0), so
+ * that v_k[x] = vscale[k] * (nibble - 8), mu[x] = mscale * (byte - 128) and
  * c_{i,k} = cscale[i] * (byte - 128).  The quantised values are those of the
  * float record's basis, coefficients and centroid.
  */

@@ -235,30 +235,49 @@ def locks_dense_decode(cfg: LocksConfig, q, k_cache, v_cache, block_table, seq_l
 # --------------------------------------------------------------------------
 def unpack_i4(raw, cfg: LocksConfig) -> Tuple:
     """Codes (unbiased int32) and scales of quantised records [..., record_bytes]
-    (layout in locks.h): mu_codes [..., d], mu_scale [...], v_codes [..., d, R],
-    v_scales [..., R], c_codes [..., B, R], c_scales [..., B]."""
+    (fragment-order layout in locks.h): mu_codes [..., d], mu_scale [...],
+    v_codes [..., d, R], v_scales [..., R], c_codes [..., B, R], c_scales [..., B]."""
     import numpy as np
     d, B, R = cfg.head_dim, cfg.page_size, cfg.rank_cap
+    KK = (R + 7) // 8
     raw = np.asarray(raw, dtype=np.uint8)
     lead = raw.shape[:-1]
     hdr = ((R + 1) * 4 + 15) // 16 * 16
     off_mq = hdr + 64 * R
     off_cq = off_mq + 128
-    off_cs = off_cq + B * R
+    off_cs = off_cq + 8 * B * KK
 
     def f32(a, b):
         return np.ascontiguousarray(raw[..., a:b]).view(np.float32)
 
     head = f32(0, 4 * (R + 1))
     v_scales, mu_scale = head[..., :R], head[..., R]
-    vb = raw[..., hdr:off_mq].reshape(*lead, R, 16, 4).astype(np.int32)   # [k][l][m]
-    lo = (vb & 15).reshape(*lead, R, 64) - 8        # v_k[4l + m]
-    hi = (vb >> 4).reshape(*lead, R, 64) - 8        # v_k[64 + 4l + m]
-    v_codes = np.swapaxes(np.concatenate([lo, hi], axis=-1), -1, -2)
-    mb = raw[..., off_mq:off_cq].reshape(*lead, 16, 2, 4).astype(np.int32)
-    mu_codes = np.concatenate([mb[..., :, 0, :].reshape(*lead, 64),
-                               mb[..., :, 1, :].reshape(*lead, 64)], axis=-1) - 128
-    c_codes = raw[..., off_cq:off_cs].reshape(*lead, B, R).astype(np.int32) - 128
+    t = np.arange(4)
+    # basis: word [k][t][j], nibble n -> (k-step 2j + (n & 3) // 2, column offset)
+    words = np.ascontiguousarray(raw[..., hdr:off_mq]).view(np.uint32).reshape(*lead, R, 4, 4)
+    v_codes = np.zeros((*lead, d, R), dtype=np.int32)
+    for n in range(8):
+        nib = ((words >> np.uint32(4 * n)) & np.uint32(15)).astype(np.int32) - 8   # [..., k, t, j]
+        step = 2 * np.arange(4)[None, :] + ((n & 3) // 2)                            # [t?, j]
+        off = (8 if (n & 1) else 0) + (1 if n >= 4 else 0)
+        cols = 16 * step + 2 * t[:, None] + off                                       # [t, j]
+        v_codes[..., cols, :] = np.moveaxis(nib, -3, -1)
+    # centroid: lane l = 4g + t -> columns 16g + 2t + (0, 1, 8, 9)
+    mb = raw[..., off_mq:off_cq].reshape(*lead, 8, 4, 4).astype(np.int32) - 128
+    mu_codes = np.zeros((*lead, d), dtype=np.int32)
+    g = np.arange(8)[:, None]
+    for e, off in enumerate((0, 1, 8, 9)):
+        mu_codes[..., 16 * g + 2 * t[None, :] + off] = mb[..., e]
+    # coefficients: cq[m][kk][l] bytes = (16m+g, 8kk+2t), (16m+g, +1), (16m+g+8, 8kk+2t), (.., +1)
+    cb = raw[..., off_cq:off_cs].reshape(*lead, B // 16, KK, 8, 4, 4).astype(np.int32) - 128
+    c_full = np.zeros((*lead, B, 8 * KK), dtype=np.int32)
+    m = np.arange(B // 16)[:, None, None, None]
+    kk = np.arange(KK)[None, :, None, None]
+    gg = np.arange(8)[None, None, :, None]
+    tt = np.arange(4)[None, None, None, :]
+    for e, (di, dk) in enumerate(((0, 0), (0, 1), (8, 0), (8, 1))):
+        c_full[..., 16 * m + gg + di, 8 * kk + 2 * tt + dk] = cb[..., e]
+    c_codes = c_full[..., :R]
     c_scales = f32(off_cs, off_cs + 4 * B)
     return mu_codes, mu_scale, v_codes, v_scales, c_codes, c_scales
 

@@ -31,6 +31,9 @@ int check_cfg(const locks_cfg_t* c) {
   if (c->head_dim != kHeadDim || (c->page_size != 64 && c->page_size != 16))
     return LOCKS_ERR_UNSUPPORTED;
   if (c->rank > 16) return LOCKS_ERR_UNSUPPORTED;
+  // the score kernel keeps a record index in an int and a page index in 24 bits
+  if (c->max_pages >= (1 << 24) || int64_t(c->num_blocks) * c->n_kv_heads >= (int64_t(1) << 31))
+    return LOCKS_ERR_UNSUPPORTED;
   if (!is_pow2_group(c->n_q_heads / c->n_kv_heads)) return LOCKS_ERR_UNSUPPORTED;
   return LOCKS_OK;
 }

@@ -114,53 +114,60 @@ __device__ __forceinline__ void write_i4_record(Smem& S, const BuildParams& prm,
   }
   __syncthreads();
   if (tid < RP * 16) {
-    // basis word (k, l): byte m = code(v_k[4l+m]) | code(v_k[64+4l+m]) << 4
-    const int k = tid >> 4, l = tid & 15;
+    // basis word vq[k][t][j]: nibbles 0/4, 1/5 = k-step 2j at columns 2t/2t+1,
+    // 2t+8/2t+9; nibbles 2/6, 3/7 = the same at k-step 2j+1 (see locks.h)
+    const int k = tid >> 4, t = (tid >> 2) & 3, j = tid & 3;
     const float sc = S.qscale[k];
+    const float* vk = Vs + k * kHeadDim;
     uint32_t w = 0;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const uint32_t lo = quant_biased(Vs[k * kHeadDim + 4 * l + m], sc, 7);
-      const uint32_t hi = quant_biased(Vs[k * kHeadDim + 64 + 4 * l + m], sc, 7);
-      w |= (lo | (hi << 4)) << (8 * m);
+    for (int h = 0; h < 2; ++h) {                         // k-step 2j + h
+      const int c0 = 16 * (2 * j + h) + 2 * t;
+      w |= quant_biased(vk[c0], sc, 7) << (4 * (2 * h));
+      w |= quant_biased(vk[c0 + 1], sc, 7) << (4 * (2 * h + 4));
+      w |= quant_biased(vk[c0 + 8], sc, 7) << (4 * (2 * h + 1));
+      w |= quant_biased(vk[c0 + 9], sc, 7) << (4 * (2 * h + 5));
     }
-    reinterpret_cast<uint32_t*>(rb + i4_vq(RP))[k * 16 + l] = w;
+    reinterpret_cast<uint32_t*>(rb + i4_vq(RP))[tid] = w;
   }
   if (tid < RP) reinterpret_cast<float*>(rb)[tid] = S.qscale[tid];
   if (tid == RP) reinterpret_cast<float*>(rb)[RP] = S.qscale[16];
-  if (tid >= 224 && tid < 240) {
-    // centroid bytes of lane l
-    const int l = tid - 224;
+  if (tid >= 224) {
+    // centroid word of lane l = 4g + t: columns 16g + 2t, +1, +8, +9
+    const int l = tid - 224, g = l >> 2, t = l & 3;
     const float sc = S.qscale[16];
-    uint32_t x = 0, y = 0;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      x |= quant_biased(S.mu[4 * l + m], sc, 127) << (8 * m);
-      y |= quant_biased(S.mu[64 + 4 * l + m], sc, 127) << (8 * m);
-    }
-    reinterpret_cast<uint2*>(rb + i4_mq(RP))[l] = make_uint2(x, y);
+    const int c0 = 16 * g + 2 * t;
+    const uint32_t w = quant_biased(S.mu[c0], sc, 127) | quant_biased(S.mu[c0 + 1], sc, 127) << 8 |
+                       quant_biased(S.mu[c0 + 8], sc, 127) << 16 |
+                       quant_biased(S.mu[c0 + 9], sc, 127) << 24;
+    reinterpret_cast<uint32_t*>(rb + i4_mq(RP))[l] = w;
   }
-  if (tid >= kBuildThreads - PB) {
-    // coefficient row i: its own scale over the r kept modes
-    const int i = tid - (kBuildThreads - PB);
-    float c[RP];
+  // coefficient rows: their scales first (one per token), then the codes in
+  // the scorer's fragment order
+  float* cs = S.A;                                           // [PB] (A is idle now)
+  auto coeff = [&](int i, int k) {
+    const float lam = k < r ? S.lam[k] : 0.f;
+    return lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
+  };
+  if (tid < PB) {
     float am = 0.f;
 #pragma unroll
-    for (int k = 0; k < RP; ++k) {
-      const float lam = k < r ? S.lam[k] : 0.f;
-      c[k] = lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
-      am = fmaxf(am, fabsf(c[k]));
-    }
+    for (int k = 0; k < RP; ++k) am = fmaxf(am, fabsf(coeff(tid, k)));
     const float sc = am > 0.f ? __fdiv_rn(am, 127.f) : 0.f;
-    uint32_t* row = reinterpret_cast<uint32_t*>(rb + i4_cq(RP) + i * RP);
-#pragma unroll
-    for (int k4 = 0; k4 < RP / 4; ++k4) {
-      uint32_t w = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) w |= quant_biased(c[4 * k4 + e], sc, 127) << (8 * e);
-      row[k4] = w;
-    }
-    reinterpret_cast<float*>(rb + i4_cscale(RP, PB))[i] = sc;
+    cs[tid] = sc;
+    reinterpret_cast<float*>(rb + i4_cscale(RP, PB))[tid] = sc;
+  }
+  __syncthreads();
+  constexpr int KK = i4_kk(RP);
+  for (int wi = tid; wi < (PB / 16) * KK * 32; wi += kBuildThreads) {
+    const int m = wi / (KK * 32), kk = (wi / 32) % KK, l = wi % 32, g = l >> 2, t = l & 3;
+    const int i0 = 16 * m + g, i1 = i0 + 8, k0 = 8 * kk + 2 * t;
+    auto code = [&](int i, int k) {
+      return k < RP ? quant_biased(coeff(i, k), cs[i], 127) : 128u;
+    };
+    const uint32_t w = code(i0, k0) | code(i0, k0 + 1) << 8 | code(i1, k0) << 16 |
+                       code(i1, k0 + 1) << 24;
+    reinterpret_cast<uint32_t*>(rb + i4_cq(RP))[wi] = w;
   }
 }
 

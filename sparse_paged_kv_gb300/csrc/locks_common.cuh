@@ -33,7 +33,8 @@ __host__ __device__ constexpr int i4_hdr(int rp) { return ((rp + 1) * 4 + 15) / 
 __host__ __device__ constexpr int i4_vq(int rp) { return i4_hdr(rp); }
 __host__ __device__ constexpr int i4_mq(int rp) { return i4_hdr(rp) + 64 * rp; }
 __host__ __device__ constexpr int i4_cq(int rp) { return i4_mq(rp) + 128; }
-__host__ __device__ constexpr int i4_cscale(int rp, int B) { return i4_cq(rp) + B * rp; }
+__host__ __device__ constexpr int i4_kk(int rp) { return (rp + 7) / 8; }
+__host__ __device__ constexpr int i4_cscale(int rp, int B) { return i4_cq(rp) + 8 * B * i4_kk(rp); }
 __host__ __device__ constexpr int i4_bytes(int rp, int B) { return i4_cscale(rp, B) + 4 * B; }
 
 // Tag type of the quantised record in the kernels' templates.
@@ -240,9 +241,10 @@ __device__ __forceinline__ float group_sum(float x) {
 
 // Online log-sum-exp state merge: (m, s) represents s * exp(m) (natural log).
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  // branch-free: with both sides empty (max -inf) the sum stays 0
   const float M = fmaxf(m, m2);
-  if (M == -INFINITY) return;
-  s = s * __expf(m - M) + s2 * __expf(m2 - M);
+  const float Mr = M == -INFINITY ? 0.f : M;
+  s = s * __expf(m - Mr) + s2 * __expf(m2 - Mr);
   m = M;
 }
 

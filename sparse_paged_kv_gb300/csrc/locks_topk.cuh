@@ -1,6 +1,6 @@
-// Warp-level selection helpers of the finalize kernel: candidate keys (share
-// bits above the inverted page id), register sorting networks over 32 lanes,
-// and a radix top-K over a shared-memory list.  Internal to the library.
+// Selection helpers of the finalize kernel: score loads, block-wide scans and
+// the block radix top-K over a shared-memory list of share bit patterns.
+// Internal to the library.
 #pragma once
 
 #include "locks_common.cuh"
@@ -34,201 +34,179 @@ __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
   return x;
 }
 
-// ---------------------------------------------------------------------------
-// register sorting networks over 32 lanes (64-bit keys, descending)
-// ---------------------------------------------------------------------------
-// Composite key of a candidate: share bits above the inverted page id, so a
-// larger key is a larger share and, between equal shares, a smaller page.
-__device__ __forceinline__ unsigned long long cand_key(uint32_t share_bits, uint32_t page) {
-  return (static_cast<unsigned long long>(share_bits) << 32) | (0xffffffffu - page);
-}
-__device__ __forceinline__ uint32_t key_page(unsigned long long k) {
-  return 0xffffffffu - static_cast<uint32_t>(k);
+constexpr int kFinThreads = 256;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kMaxSlice = 2048;              // candidates of one finalize CTA
+
+// Exclusive prefix, in thread order, of x over the block; s_warp holds
+// kFinWarps ints and must not be reused before the next block barrier.
+__device__ __forceinline__ int block_excl_scan(int x, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int inc = warp_incl_scan(x, lane);
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  int before = 0;
+#pragma unroll
+  for (int w = 0; w < kFinWarps; ++w) before += w < warp ? s_warp[w] : 0;
+  return before + inc - x;
 }
 
-__device__ __forceinline__ unsigned long long shfl_xor64(unsigned long long v, int m) {
-  return __shfl_xor_sync(kFull, v, m);
-}
-
-// Bitonic sort of one value per lane across the warp, descending in lane order.
-__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long v, int lane) {
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const unsigned long long o = shfl_xor64(v, j);
-      const bool lower = (lane & j) == 0, first_half = (lane & k) == 0 || k == 32;
-      v = (lower == first_half) ? (v > o ? v : o) : (v < o ? v : o);
-    }
-  }
-  return v;
-}
-
-// Given a bitonic sequence across the lanes, sort it descending.
-__device__ __forceinline__ unsigned long long warp_bitonic_merge_desc(unsigned long long v,
-                                                                     int lane) {
-#pragma unroll
-  for (int j = 16; j > 0; j >>= 1) {
-    const unsigned long long o = shfl_xor64(v, j);
-    v = ((lane & j) == 0) ? (v > o ? v : o) : (v < o ? v : o);
-  }
-  return v;
-}
-
-// Top 32 of two descending lane-ordered lists, descending.
-__device__ __forceinline__ unsigned long long warp_merge_top32(unsigned long long a,
-                                                              unsigned long long b, int lane) {
-  const unsigned long long br = __shfl_sync(kFull, b, 31 - lane);
-  return warp_bitonic_merge_desc(a > br ? a : br, lane);
-}
-
-// Sorts each of the 8 per-lane columns and merges them: returns the warp's
-// top 32 of its 256 keys, descending in lane order.
-__device__ __forceinline__ unsigned long long warp_top32_of_256(unsigned long long (&v)[8],
-                                                               int lane) {
-#pragma unroll
-  for (int e = 0; e < 8; ++e) v[e] = warp_sort_desc(v[e], lane);
-#pragma unroll
-  for (int e = 0; e < 8; e += 2) v[e] = warp_merge_top32(v[e], v[e + 1], lane);
-#pragma unroll
-  for (int e = 0; e < 8; e += 4) v[e] = warp_merge_top32(v[e], v[e + 2], lane);
-  return warp_merge_top32(v[0], v[4], lane);
-}
-
-// The warp's top 32 of its 256 keys, first discarding every key below the
-// smallest of the 32 lane maxima (at least 32 keys reach it, so the top 32 all
-// do); the survivors -- usually a few dozen -- are compacted through `stage`
-// (64 entries of shared memory) and sorted as two 32-lists.  More than 64
-// survivors fall back to sorting all 256.
-__device__ __forceinline__ unsigned long long warp_top32_filtered(unsigned long long (&v)[8],
-                                                                 unsigned long long* stage,
-                                                                 int lane) {
-  unsigned long long mx = v[0];
-#pragma unroll
-  for (int e = 1; e < 8; ++e) mx = v[e] > mx ? v[e] : mx;
-  unsigned long long thr = mx;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const unsigned long long x = shfl_xor64(thr, o);
-    thr = x < thr ? x : thr;
-  }
-  int mine = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) mine += v[e] >= thr;
-  const int before = warp_incl_scan(mine, lane) - mine;
-  const int total = __shfl_sync(kFull, before + mine, 31);
-  if (total > 64) return warp_top32_of_256(v, lane);
-  stage[lane] = 0ull;
-  stage[32 + lane] = 0ull;
-  __syncwarp();
-  int at = before;
-#pragma unroll
-  for (int e = 0; e < 8; ++e)
-    if (v[e] >= thr) stage[at++] = v[e];
-  __syncwarp();
-  const unsigned long long a = warp_sort_desc(stage[lane], lane);
-  const unsigned long long b = warp_sort_desc(stage[32 + lane], lane);
-  __syncwarp();
-  return warp_merge_top32(a, b, lane);
-}
-
-// Writes the first K (<= 32) keys of a descending list as pages in increasing
-// page order to out[0..K).
-__device__ __forceinline__ void warp_emit_pages_ascending(unsigned long long top, int K,
-                                                          int32_t* out, int lane) {
-  // sort the chosen pages ascending: key = inverted page (descending sort),
-  // lanes beyond K get the smallest key
-  unsigned long long pk = lane < K ? static_cast<unsigned long long>(0xffffffffu - key_page(top))
-                                   : 0ull;
-  pk = warp_sort_desc(pk, lane);
-  if (lane < K) out[lane] = int32_t(0xffffffffu - static_cast<uint32_t>(pk));
-}
-
-// ---------------------------------------------------------------------------
-// warp-level top-K over a list kept in increasing page order
-// ---------------------------------------------------------------------------
-// Chooses the K largest keys of list[0, m) (shared memory, entries in
-// increasing page order) with one warp: a 4-pass 8-bit radix select of the
-// K-th largest key in a private 256-bin histogram, then the entries above it
-// and, among the entries equal to it, the earliest (smaller pages).  The
-// chosen entries are written in list order -- still increasing page order --
-// to out_keys / out_pages; returns their number, min(K, m).
-__device__ int warp_topk(const uint32_t* keys, const int* pages, int m, int K, uint32_t* out_keys,
-                         int* out_pages, unsigned* hist) {
-  const int lane = threadIdx.x & 31;
-  if (m <= K) {
-    for (int i = lane; i < m; i += 32) { out_keys[i] = keys[i]; out_pages[i] = pages[i]; }
-    __syncwarp();
-    return m;
-  }
-  // lane l looks at entries l, l + 32, l + 64, ... (conflict-free shared loads)
-  uint32_t prefix = 0, mask = 0;
-  int kleft = K;
+// The K-th largest (1 <= K < m) of the keys keys[0..m) in shared memory.
+// Returns (T, need): that key, and how many of the keys equal to T are among
+// the K largest (at least 1).  A most-significant-bit-first search: with the
+// bits above b fixed, the block counts the keys that match them and have bit b
+// set; if fewer than the rank still wanted, T has bit b clear and those keys
+// all rank above it.  Bit 31 is clear in every key (the keys are non-negative
+// floats), so 31 counts decide T, each one warp reduction and one barrier
+// (s_cnt: two rows of kFinWarps ints, used alternately).  No histogram: keys
+// that crowd into a few values cost nothing extra.
+__device__ __forceinline__ uint2 block_radix_select(const uint32_t* keys, int m, int K,
+                                                    int (*s_cnt)[kFinWarps]) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0u;
+  int krem = K;
 #pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) hist[e * 32 + lane] = 0;
-    __syncwarp();
-    for (int i0 = 0; i0 < m; i0 += 32) {
-      // one atomic per distinct bin per round (keys crowd into a few bins)
-      const int i = i0 + lane;
-      uint32_t bin = 256u;                     // not counted
-      if (i < m) {
-        const uint32_t k = keys[i];
-        if ((k & mask) == prefix) bin = (k >> shift) & 255u;
-      }
-      const unsigned peers = __match_any_sync(kFull, bin);
-      if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], unsigned(__popc(peers)));
+  for (int b = 30; b >= 0; --b) {
+    const uint32_t hi = ~((2u << b) - 1u);       // the bits above b (fixed so far)
+    int c = 0;
+    for (int i = tid; i < m; i += kFinThreads) {
+      const uint32_t key = keys[i];
+      c += ((key & hi) == prefix && (key & (1u << b)) != 0u) ? 1 : 0;
     }
-    __syncwarp();
-    // lane l owns bins [8*(31-l), 8*(31-l)+8): lane 0 the highest
-    unsigned cnt[8], tot = 0;
+    c = __reduce_add_sync(kFull, c);
+    if (lane == 0) s_cnt[b & 1][warp] = c;
+    __syncthreads();
+    int cnt = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      cnt[e] = hist[8 * (31 - lane) + 7 - e];
-      tot += cnt[e];
-    }
-    const int incl = warp_incl_scan(int(tot), lane);
-    const int first = __ffs(__ballot_sync(kFull, incl >= kleft)) - 1;
-    int digit = 0, above = 0;
-    if (lane == first) {
-      int acc = incl - int(tot);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (acc + int(cnt[e]) >= kleft) { digit = 8 * (31 - lane) + 7 - e; above = acc; break; }
-        acc += cnt[e];
-      }
-    }
-    digit = __shfl_sync(kFull, digit, first);
-    above = __shfl_sync(kFull, above, first);
-    prefix |= uint32_t(digit) << shift;
-    mask |= 255u << shift;
-    kleft -= above;
-    __syncwarp();
+    for (int w = 0; w < kFinWarps; ++w) cnt += s_cnt[b & 1][w];
+    if (cnt >= krem) prefix |= 1u << b;
+    else krem -= cnt;
   }
-  const uint32_t thr = prefix;
-  const int need = kleft;                     // entries equal to thr to take
-  // collect in list order, 32 entries per round: ballots give the positions
-  const unsigned lt = (1u << lane) - 1;
-  int pos = 0, eq_seen = 0;
-  for (int i0 = 0; i0 < m; i0 += 32) {
-    const int i = i0 + lane;
-    const uint32_t k = i < m ? keys[i] : 0u;
-    const bool eq = i < m && k == thr;
-    const unsigned eq_bal = __ballot_sync(kFull, eq);
-    const bool take = (i < m && k > thr) || (eq && eq_seen + __popc(eq_bal & lt) < need);
-    const unsigned tb = __ballot_sync(kFull, take);
-    if (take) {
-      const int at = pos + __popc(tb & lt);
-      out_keys[at] = k;
-      out_pages[at] = pages[i];
-    }
-    pos += __popc(tb);
-    eq_seen += __popc(eq_bal);
+  return make_uint2(prefix, uint32_t(krem));
+}
+
+// Calls put(i, pos) for the entries of the K largest keys -- every key above T
+// and the first `need` keys equal to T -- in index order, pos = 0, 1, ...
+// Each thread takes a contiguous run of entries; one block scan of the
+// packed counts (above T in the high 16 bits, equal in the low) places it.
+template <typename F>
+__device__ __forceinline__ void block_emit_topk(const uint32_t* keys, int m, uint32_t T, int need,
+                                                int* s_warp, F&& put) {
+  const int tid = threadIdx.x;
+  const int per = (m + kFinThreads - 1) / kFinThreads;
+  const int i0 = min(m, tid * per), i1 = min(m, i0 + per);
+  int gt = 0, eq = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = keys[i];
+    gt += key > T ? 1 : 0;
+    eq += key == T ? 1 : 0;
   }
-  __syncwarp();
-  return K;
+  const int ex = block_excl_scan((gt << 16) | eq, s_warp);
+  int ties = ex & 0xffff;
+  int pos = (ex >> 16) + min(ties, need);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = keys[i];
+    bool take = key > T;
+    if (key == T) {
+      take = ties < need;
+      ++ties;
+    }
+    if (take) put(i, pos++);
+  }
+}
+
+constexpr int kSurvCap = 1024;               // survivors the ranking path holds
+
+// Shared-memory scratch of block_topk.
+struct TopkScratch {
+  uint32_t wj[kFinWarps];                    // per warp: its j-th largest thread maximum
+  uint32_t sk[kSurvCap];                     // survivors: key
+  int si[kSurvCap];                          //            index
+  int scan[6][kFinWarps];
+};
+
+// Calls put(i, pos) for the K largest (1 <= K < m, K <= kFinThreads) of the
+// keys keys[0..m) in shared memory -- ordered by key, then by smaller index --
+// in index order, pos = 0, 1, ...
+//
+// Each thread takes a contiguous run of the keys.  With j = ceil(K / 8), the
+// smallest over the 8 warps of each warp's j-th largest thread maximum is a
+// lower bound of the K-th largest key (8j >= K keys reach it); only keys at
+// or above it survive, usually a few dozen.  The survivors,
+// compacted in index order, are ranked against one another directly and the
+// winners placed by one block scan -- a handful of barriers in all.  When
+// more survive than kSurvCap holds (many equal keys), the bit-by-bit search
+// of the K-th key decides instead.
+template <typename F>
+__device__ __forceinline__ void block_topk(const uint32_t* keys, int m, int K, TopkScratch& S,
+                                           F&& put) {
+  const int tid = threadIdx.x;
+  const int per = (m + kFinThreads - 1) / kFinThreads;
+  const int i0 = min(m, tid * per), i1 = min(m, i0 + per);
+  uint32_t mx = 0u;                            // a thread without keys: 0, which
+  for (int i = i0; i < i1; ++i) mx = max(mx, keys[i]);   // only lets every key through
+  {
+    // rank of this lane's maximum in its warp (ties: lower lane first)
+    const int lane = tid & 31, j = (K + kFinWarps - 1) / kFinWarps;
+    int r = 0;
+#pragma unroll 4
+    for (int d = 1; d < 32; ++d) {
+      const int o_lane = (lane + d) & 31;
+      const uint32_t o = __shfl_sync(kFull, mx, o_lane);
+      r += (o > mx || (o == mx && o_lane < lane)) ? 1 : 0;
+    }
+    if (r == j - 1) S.wj[tid >> 5] = mx;
+  }
+  __syncthreads();
+  uint32_t lb = S.wj[0];
+#pragma unroll
+  for (int w = 1; w < kFinWarps; ++w) lb = min(lb, S.wj[w]);
+  int c = 0;
+  for (int i = i0; i < i1; ++i) c += keys[i] >= lb ? 1 : 0;
+  int n_surv = 0;
+  {
+    const int lane = tid & 31, warp = tid >> 5;
+    const int inc = warp_incl_scan(c, lane);
+    if (lane == 31) S.scan[0][warp] = inc;
+    __syncthreads();
+    int before = 0;
+#pragma unroll
+    for (int w = 0; w < kFinWarps; ++w) {
+      const int x = S.scan[0][w];
+      before += w < warp ? x : 0;
+      n_surv += x;
+    }
+    if (n_surv <= kSurvCap) {
+      int at = before + inc - c;
+      for (int i = i0; i < i1; ++i)
+        if (keys[i] >= lb) { S.sk[at] = keys[i]; S.si[at] = i; ++at; }
+    }
+  }
+  if (n_surv > kSurvCap) {
+    const uint2 sel = block_radix_select(keys, m, K, S.scan + 1);
+    block_emit_topk(keys, m, sel.x, int(sel.y), S.scan[3], put);
+    return;
+  }
+  __syncthreads();
+  // rank every survivor; winners are those of rank < K.  Thread t takes a
+  // contiguous run of survivors so that one scan places the winners in order.
+  const int ps = (n_surv + kFinThreads - 1) / kFinThreads;
+  const int j0 = min(n_surv, tid * ps), j1 = min(n_surv, j0 + ps);
+  uint32_t win = 0u;                           // bit q: survivor j0 + q wins (ps <= 4)
+  int nw = 0;
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t kj = S.sk[j];
+    int r = 0;
+    for (int q = 0; q < n_surv; ++q) {
+      const uint32_t o = S.sk[q];
+      r += (o > kj || (o == kj && q < j)) ? 1 : 0;
+    }
+    if (r < K) { win |= 1u << (j - j0); ++nw; }
+  }
+  const int pos0 = block_excl_scan(nw, S.scan[4]);
+  int pos = pos0;
+  for (int j = j0; j < j1; ++j)
+    if (win & (1u << (j - j0))) put(S.si[j], pos++);
 }
 
 }  // namespace

@@ -144,37 +144,57 @@ def test_unpack_records_layout():
 
 
 def test_unpack_i4_layout(lib):
-    """The quantised record layout documented in locks.h, packed here by hand,
-    unpacks to the codes and scales it was packed from."""
+    """The quantised record layout documented in locks.h, packed here by hand
+    from its description, unpacks to the codes and scales it was packed from."""
     import numpy as np
-    c = cfg(summary_dtype=B.LOCKS_SUMMARY_I4, rank=8)
-    R, Bp, d = c.rank_cap, c.page_size, c.head_dim
-    nbytes = B.summary_record_bytes(c)
-    hdr = ((R + 1) * 4 + 15) // 16 * 16
-    assert nbytes == hdr + 64 * R + 128 + Bp * R + 4 * Bp
-    rng = np.random.default_rng(3)
-    v = rng.integers(-7, 8, (d, R))
-    mu = rng.integers(-127, 128, d)
-    cc = rng.integers(-127, 128, (Bp, R))
-    vs = rng.random(R).astype(np.float32)
-    cs = rng.random(Bp).astype(np.float32)
-    rec = np.zeros(nbytes, np.uint8)
-    rec[:4 * R] = vs.view(np.uint8)
-    rec[4 * R:4 * R + 4] = np.float32(0.25).reshape(1).view(np.uint8)
-    for k in range(R):
-        for l in range(16):
-            for m in range(4):
-                rec[hdr + (k * 16 + l) * 4 + m] = (v[4 * l + m, k] + 8) | ((v[64 + 4 * l + m, k] + 8) << 4)
-    for l in range(16):
-        for m in range(4):
-            rec[hdr + 64 * R + l * 8 + m] = mu[4 * l + m] + 128
-            rec[hdr + 64 * R + l * 8 + 4 + m] = mu[64 + 4 * l + m] + 128
-    rec[hdr + 64 * R + 128:hdr + 64 * R + 128 + Bp * R] = (cc + 128).reshape(-1)
-    rec[hdr + 64 * R + 128 + Bp * R:] = cs.view(np.uint8)
-    mu_c, mu_s, v_c, v_s, c_c, c_s = B.unpack_i4(rec[None], c)
-    assert np.array_equal(mu_c[0], mu) and float(mu_s[0]) == 0.25
-    assert np.array_equal(v_c[0], v) and np.array_equal(v_s[0], vs)
-    assert np.array_equal(c_c[0], cc) and np.array_equal(c_s[0], cs)
-    m, V, C = B.unpack_records(rec[None], c)
-    assert np.allclose(V[0], v * vs[None, :]) and np.allclose(C[0], cc * cs[:, None])
-    assert np.allclose(m[0], mu * 0.25)
+    for rank, Bp in ((8, 64), (16, 16), (3, 64)):
+        c = cfg(summary_dtype=B.LOCKS_SUMMARY_I4, rank=rank, page_size=Bp)
+        R, d = c.rank_cap, c.head_dim
+        KK = (R + 7) // 8
+        nbytes = B.summary_record_bytes(c)
+        hdr = ((R + 1) * 4 + 15) // 16 * 16
+        assert nbytes == hdr + 64 * R + 128 + 8 * Bp * KK + 4 * Bp
+        rng = np.random.default_rng(3 + rank)
+        v = rng.integers(-7, 8, (d, R))
+        mu = rng.integers(-127, 128, d)
+        cc = rng.integers(-127, 128, (Bp, R))
+        vs = rng.random(R).astype(np.float32)
+        cs = rng.random(Bp).astype(np.float32)
+        rec = np.zeros(nbytes, np.uint8)
+        rec[:4 * R] = vs.view(np.uint8)
+        rec[4 * R:4 * R + 4] = np.float32(0.25).reshape(1).view(np.uint8)
+        words = np.zeros((R, 4, 4), np.uint32)
+        for k in range(R):
+            for t in range(4):
+                for j in range(4):
+                    w = 0
+                    for h in range(2):                  # k-step 2j + h
+                        c0 = 16 * (2 * j + h) + 2 * t
+                        w |= int(v[c0, k] + 8) << (4 * (2 * h))
+                        w |= int(v[c0 + 1, k] + 8) << (4 * (2 * h + 4))
+                        w |= int(v[c0 + 8, k] + 8) << (4 * (2 * h + 1))
+                        w |= int(v[c0 + 9, k] + 8) << (4 * (2 * h + 5))
+                    words[k, t, j] = w
+        rec[hdr:hdr + 64 * R] = words.reshape(-1).view(np.uint8)
+        for l in range(32):
+            g, t = l >> 2, l & 3
+            for e, off in enumerate((0, 1, 8, 9)):
+                rec[hdr + 64 * R + 4 * l + e] = mu[16 * g + 2 * t + off] + 128
+        base = hdr + 64 * R + 128
+        for m in range(Bp // 16):
+            for kk in range(KK):
+                for l in range(32):
+                    g, t = l >> 2, l & 3
+                    for e, (di, dk) in enumerate(((0, 0), (0, 1), (8, 0), (8, 1))):
+                        k = 8 * kk + 2 * t + dk
+                        val = cc[16 * m + g + di, k] if k < R else 0
+                        rec[base + ((m * KK + kk) * 32 + l) * 4 + e] = val + 128
+        rec[base + 8 * Bp * KK:] = cs.view(np.uint8)
+        mu_c, mu_s, v_c, v_s, c_c, c_s = B.unpack_i4(rec[None], c)
+        assert np.array_equal(mu_c[0], mu) and float(mu_s[0]) == 0.25
+        assert np.array_equal(v_c[0], v) and np.array_equal(v_s[0], vs)
+        assert np.array_equal(c_c[0], cc) and np.array_equal(c_s[0], cs)
+        m_, V, C = B.unpack_records(rec[None], c)
+        assert np.allclose(V[0], (v * vs[None, :])[:, :rank])
+        assert np.allclose(C[0], (cc * cs[:, None])[:, :rank])
+        assert np.allclose(m_[0], mu * 0.25)
