@@ -134,6 +134,17 @@ __global__ void __launch_bounds__(kDecThreads)
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_v) : "memory");
   }
 
+  // this sequence's block-table row and length are pulled into L2 while the
+  // previous kernel finishes (prefetches return no data, so a writer that is
+  // still running cannot be raced), for the page lookups after the wait
+  {
+    const int32_t* row = p.block_table + size_t(b) * p.max_pages;
+    const int lines = (p.max_pages + 31) / 32;     // 128-byte lines of the row
+    for (int l = tid; l < lines; l += kDecThreads)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 32 * l));
+    if (tid == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.seq_lens + b));
+  }
+
   // launched as a programmatic dependent of the previous kernel on the stream:
   // wait for it to finish before reading anything it may have written
   asm volatile("griddepcontrol.wait;" ::: "memory");

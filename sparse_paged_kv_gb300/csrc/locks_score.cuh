@@ -606,9 +606,11 @@ __global__ void __launch_bounds__(kSelThreads, (!std::is_same_v<T, I4Rec> &&
 
 template <int G, int RP, typename T, int PB>
 int launch_score_t(const SelectParams& p, int n_ctas, cudaStream_t stream) {
-  // ring depth: enough record bytes in flight per warp to cover the memory
-  // latency (a quantised record is about a fifth of a float one)
-  constexpr int STAGES = std::is_same_v<T, I4Rec> ? 4 : 2;
+  // ring depth: two page pairs per warp.  Deeper rings (tried for the small
+  // quantised record) only make the opening burst of copies longer: every
+  // warp's first pair then lands later, and the tensor-core scoring, which
+  // takes about as long as the copies, starts later.
+  constexpr int STAGES = 2;
   const size_t smem = size_t(kSelWarps) * STAGES * 2 * p.rec_bytes +
                       kSelWarps * STAGES * sizeof(uint64_t) +
                       kSelWarps * 2 * pbuf_stride<G, RP, T>() * sizeof(float) +

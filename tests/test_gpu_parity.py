@@ -32,7 +32,7 @@ CASES = {
     # more than 2048 candidates: several finalize slices, merged by the last one
     "slices3": TINY.with_(context=64 * 4200 + 11, global_rank=16, carrier_count=None,
                           carrier_frac=0.01, budget_tokens=2048, seed=2014),
-    # k - 2 > 32: the radix top-k path, with one and with several slices
+    # k - 2 > 32, with one and with several slices
     "k40": TINY.with_(context=64 * 300, budget_tokens=64 * 40, seed=2015),
     "k40_slices3": TINY.with_(context=64 * 4200, budget_tokens=64 * 40, global_rank=16,
                               seed=2016),
@@ -47,7 +47,7 @@ CASES = {
     # 80 units: three splits per unit, merged through a thread-block cluster
     "cluster_merge": TINY.with_(batch=40, context=64 * 20 + 5, seed=2030),
     "b16_cluster_merge": TINY.with_(page_size=16, batch=40, context=16 * 40 + 3, seed=2031),
-    # Llama layer shape at B = 16: k = 128 (radix top-k)
+    # Llama layer shape at B = 16: k = 128
     "b16_gqa4_k128": TINY.with_(page_size=16, batch=2, n_q_heads=32, n_kv_heads=8,
                                 context=16384, budget_tokens=2048, global_rank=16,
                                 carrier_count=None, carrier_frac=0.01, seed=2024),
@@ -240,3 +240,32 @@ def test_graph_replay_matches_eager_and_oracle():
             P.compare_sparse_decode(layer, inputs2, snap2, res, rep2)
         rep2.check()
     assert int(layer.status.cpu()[0]) == 0
+
+
+@pytest.mark.parametrize("summary_dtype", [0, 2])
+@pytest.mark.parametrize("context", [64 * 1500 + 9, 64 * 4200 + 11])
+def test_equal_shares_select_the_smallest_pages(context, summary_dtype):
+    """With zero queries every logit is 0, so every complete page has the same
+    s_hat and the same share: the selection is then decided by the tie rule
+    alone (between equal shares the smaller page), i.e. pages 1 .. k-2 besides
+    the forced ones.  1499 candidates in one slice, or three slices of up to
+    2048, leave more equal keys above the top-K's lower bound than its ranking
+    buffer holds, so the bit-by-bit search decides; the slices' winners are
+    then merged through the ranking path."""
+    import torch
+    from sparse_paged_kv_gb300 import runtime
+    w = TINY.with_(context=context, seed=2040)
+    gen = W.generate(w)
+    inputs = dataclasses.replace(gen, q=np.zeros_like(gen.q))
+    layer = runtime.LocksLayer.from_inputs(inputs, summary_dtype=summary_dtype)
+    layer.build()
+    layer.select()
+    torch.cuda.synchronize()
+    assert int(layer.status.cpu()[0]) == 0
+    sel = layer.selected.cpu().numpy()
+    k = O.page_budget(w.budget_tokens, w.page_size)
+    for b in range(w.batch):
+        n = -(-int(inputs.seq_lens[b]) // w.page_size)
+        expect = [0] + list(range(1, k - 1)) + [n - 1]
+        for h in range(w.n_kv_heads):
+            assert list(sel[b, h]) == expect, (b, h, list(sel[b, h]))
