@@ -83,9 +83,12 @@ struct BuildParams {
 
 // ctas_per_sm: score CTAs per SM the grid is sized for (see score_ctas_per_sm)
 SelectGeom select_geometry(int units, int max_pages, int G, int k, int ctas_per_sm);
-// Score CTAs per SM for a summary type: 4 for the quantised record (small
-// records, denser arithmetic: more warps to hide instruction latency), else 2.
-inline int score_ctas_per_sm(int summary_dtype) { return summary_dtype == LOCKS_SUMMARY_I4 ? 4 : 2; }
+// Score CTAs per SM the grid is sized for.  Quantised records: 4, all
+// resident at once (small records, denser arithmetic: more warps to hide
+// instruction latency).  Float records: 2 resident per SM, in two waves, so
+// that SMs that stream faster (HBM bandwidth per SM differs across the chip)
+// take more of the second wave.
+inline int score_ctas_per_sm(int /*summary_dtype*/) { return 4; }
 // score kernel only, one definition per page size (locks_select.cu: 64,
 // locks_score_b16.cu: 16)
 int launch_score_b64(const SelectParams& p, int G, int RP, int dtype, int n_ctas,

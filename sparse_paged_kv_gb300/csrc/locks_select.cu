@@ -82,24 +82,28 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
     }
   }
 
-  // ---- log Z_g from the unit's partials: every warp merges the (max, sum) ---
-  // pairs itself, so no block barrier separates log Z from the shares: each
-  // lane merges its segments, then the warp takes the largest max, rescales
-  // every lane's sum to it once and adds the sums
+  // ---- log Z_g from the unit's partials ---------------------------------------
+  // Up to 128 segments: every warp merges them itself, so no block barrier
+  // separates log Z from the shares.  More (long sequences): the block shares
+  // the loads -- one round of them -- and combines the warps' results through
+  // shared memory.  Either way each lane merges its segments, then the warp
+  // takes the largest max, rescales every lane's sum to it once and adds.
   float lz[G];
   {
     const int i_first = int((long(u) * p.mc) / p.per_cta);
     const int i_last = int((long(u + 1) * p.mc - 1) / p.per_cta);
     const int nseg = (i_last - i_first + 1) * 4;
+    const bool wide = nseg > 128;
+    const int stride = wide ? kFinThreads : 32, first = wide ? tid : lane;
     float m[G], s[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) { m[g] = -INFINITY; s[g] = 0.f; }
-    // four segments per lane in flight at once, then merged
-    for (int sg0 = 0; sg0 < nseg; sg0 += 128) {
+    // four segments per thread in flight at once, then merged
+    for (int sg0 = 0; sg0 < nseg; sg0 += 4 * stride) {
       float2 v[4][G];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int sg = sg0 + 32 * r + lane;
+        const int sg = sg0 + stride * r + first;
 #pragma unroll
         for (int g = 0; g < G; ++g)
           v[r][g] = sg < nseg ? __ldcg(p.ws_part + (size_t(u) * p.nseg_max + sg) * G + g)
@@ -122,8 +126,27 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
       float x = (m[g] == -INFINITY) ? 0.f : s[g] * __expf(m[g] - M);
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
-      lz[g] = (x > 0.f && M != -INFINITY) ? M + kLn2 * lg2_approx(x) : -INFINITY;
+      m[g] = M;
+      s[g] = x;
     }
+    if (wide) {
+      __shared__ float2 s_wz[kFinWarps][8];
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) s_wz[tid >> 5][g] = make_float2(m[g], s[g]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        s[g] = 0.f;
+#pragma unroll
+        for (int w = 0; w < kFinWarps; ++w) lse_merge(m[g], s[g], s_wz[w][g].x, s_wz[w][g].y);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      lz[g] = (s[g] > 0.f && m[g] != -INFINITY) ? m[g] + kLn2 * lg2_approx(s[g]) : -INFINITY;
   }
 
   // ---- averaged shares m_bar of this slice's candidates (Cor. 3) ------------
@@ -163,6 +186,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   auto topk = [&](int m, int KK, auto put) {
     if (KK >= m) {
       for (int i = tid; i < m; i += kFinThreads) put(i, i);
+    } else if (m <= kFinThreads) {
+      block_topk_small(keys, m, KK, ts.scan[5], put);
     } else {
       block_topk(keys, m, KK, ts, put);
     }
@@ -182,19 +207,15 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   __syncthreads();
   if (!s_is_last) return;
   __threadfence();
-  // slice s2 holds min(K, its candidates) winners in page order; concatenated
-  // in slice order the list stays in page order
-  int m_all = 0;
-  for (int s2 = 0; s2 < nsl; ++s2) {
-    const int cs = min(n_cand, (s2 + 1) * p.slice) - s2 * p.slice;
-    const int w = min(K, cs);
-    const uint2* src = p.ws_cand + (size_t(u) * p.nslices_max + s2) * p.cand_per_slice;
-    for (int i = tid; i < w; i += kFinThreads) {
-      const uint2 e = __ldcg(src + i);
-      keys[m_all + i] = e.x;
-      pages[m_all + i] = int(e.y);
-    }
-    m_all += w;
+  // slice s2 holds min(K, its candidates) winners in page order: K for every
+  // slice but the last, so entry i of the concatenation (slice order, still
+  // page order) is entry i % K of slice i / K.  All of them load at once.
+  const int m_all = (nsl - 1) * K + min(K, n_cand - (nsl - 1) * p.slice);
+  for (int i = tid; i < m_all; i += kFinThreads) {
+    const int s2 = i / K, e2 = i - s2 * K;
+    const uint2 e = __ldcg(p.ws_cand + (size_t(u) * p.nslices_max + s2) * p.cand_per_slice + e2);
+    keys[i] = e.x;
+    pages[i] = int(e.y);
   }
   __syncthreads();
   topk(m_all, K, [=](int i, int pos) { out[1 + pos] = pages[i]; });

@@ -115,6 +115,28 @@ __device__ __forceinline__ void block_emit_topk(const uint32_t* keys, int m, uin
   }
 }
 
+// Calls put(i, pos) for the K largest (1 <= K < m <= kFinThreads) of the keys
+// keys[0..m) -- ordered by key, then by smaller index -- in index order:
+// thread i ranks key i against all m keys directly, one scan places the
+// winners.  For short lists this beats bounding and compacting first.
+template <typename F>
+__device__ __forceinline__ void block_topk_small(const uint32_t* keys, int m, int K, int* s_warp,
+                                                 F&& put) {
+  const int tid = threadIdx.x;
+  bool win = false;
+  if (tid < m) {
+    const uint32_t mine = keys[tid];
+    int r = 0;
+    for (int j = 0; j < m; ++j) {
+      const uint32_t o = keys[j];
+      r += (o > mine || (o == mine && j < tid)) ? 1 : 0;
+    }
+    win = r < K;
+  }
+  const int pos = block_excl_scan(win ? 1 : 0, s_warp);
+  if (win) put(tid, pos);
+}
+
 constexpr int kSurvCap = 1024;               // survivors the ranking path holds
 
 // Shared-memory scratch of block_topk.
