@@ -36,6 +36,11 @@ CASES = {
     "k40": TINY.with_(context=64 * 300, budget_tokens=64 * 40, seed=2015),
     "k40_slices3": TINY.with_(context=64 * 4200, budget_tokens=64 * 40, global_rank=16,
                               seed=2016),
+    # G = 8 with k - 2 > 32 over three slices; G = 1 over two (finalize
+    # register pressure and the slice merge at the group-size extremes)
+    "group8_k40_slices3": TINY.with_(n_q_heads=16, n_kv_heads=2, context=64 * 4200 + 11,
+                                     budget_tokens=64 * 40, seed=2017),
+    "group1_slices2": TINY.with_(n_q_heads=2, n_kv_heads=2, context=64 * 2600 + 5, seed=2018),
     # page size 16 (four pages per decode stage)
     "b16": TINY.with_(page_size=16, seed=2020),
     "b16_ragged": TINY.with_(page_size=16, batch=5, seq_lens=(4096 + 7, 200, 16 * 33, 9, 0),
