@@ -13,6 +13,14 @@ exact per-head page masses s_j = log sum_i exp(q^T k_i / sqrt d)):
               selection S*;
 * needle   -- planted carrier pages kept, conditional on S* keeping them.
 
+Rival selectors for comparison (scored here from the keys, like the exact
+ceiling; they are not part of the product path): "centroid-only" scores a page
+as if every token were its centroid, log nv + q.mu/sqrt(d), a lower bound of
+the exact log-mass by Jensen's inequality; "Quest" scores it by the elementwise
+key envelope of Lemma 2, log nv + sum_d max(q_d min_d, q_d max_d)/sqrt(d), an
+upper bound of every logit and so of the log-mass.  Both then go through the
+same shares, share-average and forced-page top-(k-2) as Locks.
+
 Table D.17 (App. D) compares GQA combine rules on the exact per-head shares:
 share-average (the shipped rule, Cor. 3), group-max, group-mass, and a
 per-head oracle (each head its own selection); per head the coverage is the
@@ -53,6 +61,38 @@ def unit_exact(inputs, b: int, h: int) -> Dict:
     best = O.select_from_shares(mbar, cand, forced, n, k)
     return {"s": s, "forced": forced, "cand": cand, "k": k, "n": n, "best": best,
             "carriers": np.asarray(inputs.carriers[b][h], dtype=np.int64)}
+
+
+def rival_log_mass(inputs, b: int, h: int, rule: str) -> np.ndarray:
+    """Per-head page scores [G][n] of a rival selector on the log-mass scale
+    (-inf for pages without valid tokens): rule "centroid" or "quest"."""
+    w = inputs.workload
+    B, G, d = w.page_size, w.group, w.head_dim
+    t = int(inputs.seq_lens[b])
+    n = -(-t // B)
+    q = O.bf16_to_f64(inputs.q[b, h * G:(h + 1) * G])          # [G][d]
+    s = np.full((G, n), -np.inf)
+    for j in range(n):
+        nv = O.valid_tokens(t, B, j)
+        if nv <= 0:
+            continue
+        k = O.page_keys(inputs.k_cache, inputs.block_table, b, h, j, nv)   # [nv][d]
+        if rule == "centroid":
+            s[:, j] = np.log(nv) + (q @ k.mean(axis=0)) / np.sqrt(d)
+        elif rule == "quest":
+            lo, hi = k.min(axis=0), k.max(axis=0)
+            s[:, j] = np.log(nv) + np.maximum(q * lo, q * hi).sum(axis=1) / np.sqrt(d)
+        else:
+            raise ValueError(rule)
+    return s
+
+
+def rival_selection(ex: Dict, s_rival: np.ndarray):
+    """The forced pages plus the top-(k-2) candidates by the share-average of a
+    rival selector's per-head scores."""
+    cand = ex["cand"]
+    mbar = O.share_average(O.page_shares(s_rival[:, cand]))
+    return O.select_from_shares(mbar, cand, ex["forced"], ex["n"], ex["k"])
 
 
 def _mass(s: np.ndarray, pages) -> np.ndarray:

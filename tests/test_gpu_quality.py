@@ -1,9 +1,15 @@
 """Selection fidelity of the GPU selections on a synthetic Llama-layer
 workload (Table B.1 and Table D.17 statistics of the Locks paper; see
-tests/quality.py).  Asserted: what holds by construction or is proven -- the
-exact selection scores 1 against itself, share-average has the largest mean
-contested coverage among shared selections (Cor. 3), the per-head oracle
-bounds every shared rule head by head on average.  The rest is reported."""
+tests/quality.py), with a rank sweep of the GPU summaries (r = 2, 4, 8, 15,
+Table D.12's ranks) and the centroid-only and Quest rival selectors beside
+them, and a second workload whose carriers are single "peaky" tokens.
+Asserted: what holds by construction or is proven -- the exact selection
+scores 1 against itself, share-average has the largest mean contested
+coverage among shared selections (Cor. 3), the per-head oracle bounds every
+shared rule head by head on average, and the rivals' scores bracket the exact
+page log-mass.  The rest is reported."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -14,6 +20,10 @@ pytestmark = pytest.mark.gpu
 
 # Llama-3.1-8B layer shape, two sequences of 32K tokens, b = 2048 (k = 32)
 WQ = W.get("llama32k").with_(batch=2, seed=3001)
+# the same with single-token carriers: one key of each carrier page shifted by
+# 4 along the group query direction (its page's centroid moves by 4/64)
+WP = W.get("llama32k").with_(batch=2, carrier_token=True, carrier_bias=4.0, seed=3002)
+RANKS = (2, 4, 8, 15)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -39,6 +49,37 @@ def _gpu_selection(inputs, summary_dtype):
     return sel
 
 
+def _rank_sweep_and_rivals(inputs, units, ex, rows):
+    """Rows of the GPU rank sweep (fp32 records) and of the two rival
+    selectors; checks that the rivals' scores bracket the exact log-mass."""
+    from sparse_paged_kv_gb300 import binding as Bd
+    w = inputs.workload
+    for r in RANKS:
+        inp_r = dataclasses.replace(inputs, workload=w.with_(rank=r))
+        sel = _gpu_selection(inp_r, Bd.LOCKS_SUMMARY_F32)
+        rows[f"Locks r{r} (fp32 record)"] = [Q.unit_stats(ex[(b, h)], sel[b, h]) for b, h in units]
+    for rule, name in (("centroid", "centroid-only"), ("quest", "Quest envelope")):
+        stats = []
+        for b, h in units:
+            s_r = Q.rival_log_mass(inputs, b, h, rule)
+            s_x = ex[(b, h)]["s"]
+            ok = np.isfinite(s_x)
+            if rule == "centroid":
+                assert np.all(s_r[ok] <= s_x[ok] + 1e-9)
+            else:
+                assert np.all(s_r[ok] >= s_x[ok] - 1e-9)
+            stats.append(Q.unit_stats(ex[(b, h)], Q.rival_selection(ex[(b, h)], s_r)))
+        rows[name] = stats
+
+
+def _print_table(title, table):
+    print(title)
+    for name, t in table.items():
+        needle = "n/a" if t["needle"] is None else f"{100 * t['needle']:.1f}"
+        print(f"  {name:32s} gamma_c {100 * t['gamma_c']:5.1f}  gamma {100 * t['gamma']:5.1f}  "
+              f"recall {100 * t['recall']:5.1f}  needle {needle}")
+
+
 def test_selection_fidelity():
     from sparse_paged_kv_gb300 import binding as Bd
     inputs = W.generate(WQ)
@@ -46,19 +87,15 @@ def test_selection_fidelity():
     units = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
     ex = {u: Q.unit_exact(inputs, *u) for u in units}
     sels = {name: _gpu_selection(inputs, dt) for name, dt in
-            (("Locks r8fp (fp32 record)", Bd.LOCKS_SUMMARY_F32),
-             ("Locks r8 bf16 record", Bd.LOCKS_SUMMARY_BF16),
+            (("Locks r8 bf16 record", Bd.LOCKS_SUMMARY_BF16),
              ("Locks r8i4 (quantised record)", Bd.LOCKS_SUMMARY_I4))}
     rows = {"exact LSE (ceiling)": [Q.unit_stats(ex[u], ex[u]["best"]) for u in units]}
+    _rank_sweep_and_rivals(inputs, units, ex, rows)
     for name, sel in sels.items():
         rows[name] = [Q.unit_stats(ex[(b, h)], sel[b, h]) for b, h in units]
     table = {name: Q.aggregate(r) for name, r in rows.items()}
-    print(f"\nselection fidelity, {w.name} x{w.batch}, b = {w.budget_tokens} "
-          f"(k = {ex[units[0]]['k']} of {ex[units[0]]['n']} pages)")
-    for name, t in table.items():
-        needle = "n/a" if t["needle"] is None else f"{100 * t['needle']:.1f}"
-        print(f"  {name:32s} gamma_c {100 * t['gamma_c']:5.1f}  gamma {100 * t['gamma']:5.1f}  "
-              f"recall {100 * t['recall']:5.1f}  needle {needle}")
+    _print_table(f"\nselection fidelity, {w.name} x{w.batch}, b = {w.budget_tokens} "
+                 f"(k = {ex[units[0]]['k']} of {ex[units[0]]['n']} pages)", table)
     ceil = table["exact LSE (ceiling)"]
     assert ceil["recall"] == 1.0 and ceil["needle"] in (1.0, None)
 
@@ -78,3 +115,22 @@ def test_selection_fidelity():
     # each head's own top set bounds any shared set on that head
     for u_sa, u_ph in zip(per_unit["share-average"], per_unit["per-head"]):
         assert np.all(u_ph >= u_sa - 1e-12)
+
+
+def test_peaky_carriers():
+    """Carriers that are a single strongly attended token: the exact
+    selection keeps them (the bias was chosen for that); the table reports how
+    Locks at each rank, centroid-only and Quest fare on them."""
+    from sparse_paged_kv_gb300 import binding as Bd
+    inputs = W.generate(WP)
+    w = inputs.workload
+    units = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
+    ex = {u: Q.unit_exact(inputs, *u) for u in units}
+    rows = {"exact LSE (ceiling)": [Q.unit_stats(ex[u], ex[u]["best"]) for u in units]}
+    _rank_sweep_and_rivals(inputs, units, ex, rows)
+    sel = _gpu_selection(inputs, Bd.LOCKS_SUMMARY_I4)
+    rows["Locks r8i4 (quantised record)"] = [Q.unit_stats(ex[(b, h)], sel[b, h]) for b, h in units]
+    table = {name: Q.aggregate(r) for name, r in rows.items()}
+    _print_table(f"\npeaky carriers (one token of each carrier page shifted by "
+                 f"{w.carrier_bias}), {w.name} x{w.batch}", table)
+    assert table["exact LSE (ceiling)"]["needle"] == 1.0

@@ -5,7 +5,9 @@ query/KV heads, head dimension, page size B, context T, summary rank r, token
 budget b) and the recipe of its synthetic keys: per page a rank-8 product
 A_p G_p with A_p, G_p ~ N(0,1)/sqrt(8), isotropic noise, optionally a shared
 global rank-16 component, and a few "carrier" pages whose keys are shifted by
-0.5 times the unit direction of the GQA group's summed query.
+0.5 times the unit direction of the GQA group's summed query (or, with
+carrier_token, a single token of each carrier page shifted by carrier_bias:
+a "peaky" needle that moves the page centroid by only 1/B of that).
 
 The shapes follow the layer shapes of the models the Locks paper evaluates on
 (Llama-3.1-8B: 32 query / 8 KV heads; Qwen3-4B: 32 / 8; head_dim 128) and its
@@ -42,6 +44,7 @@ class LocksWorkload:
     carrier_count: Optional[int] = None   # carriers per (sequence, KV head); overrides carrier_frac
     carrier_frac: float = 0.0         # fraction of candidate pages made carriers (rounded up)
     carrier_bias: float = 0.5         # shift of every key of a carrier page along the group query direction
+    carrier_token: bool = False       # shift one (seeded) token of each carrier page instead of every key
     seed: int = 1000
     seq_lens: Optional[Tuple[int, ...]] = None   # ragged per-sequence lengths (overrides context)
     spare_blocks: int = 3             # unused physical blocks in the pool (filled with NaN)

@@ -18,8 +18,10 @@ Key recipe per (sequence, KV head), page by page:
     + noise * N(0,1)
     + Z_t H    (shared global rank-16 part, Z: T x 16, H: 16 x d, N(0,1)/4)
     + 0.5 * q_hat on every key of a carrier page,
-where q_hat is the unit vector of the sum of the GQA group's queries.  Values
-and queries are N(0,1).
+where q_hat is the unit vector of the sum of the GQA group's queries.  With
+``carrier_token`` only one seeded token of each carrier page gets the shift
+(``carrier_bias`` * q_hat), so the page's centroid barely moves.  Values and
+queries are N(0,1).
 
 Nothing in this module computes any part of the Locks method.
 """
@@ -94,6 +96,10 @@ def _gen_unit(w: LocksWorkload, b: int, h: int, seq_len: int, q_hat: np.ndarray,
     carriers = np.sort(rng.choice(cand, size=n_car, replace=False)) if n_car else np.zeros(0, np.int64)
     is_carrier = np.zeros(n_pages, dtype=bool)
     is_carrier[carriers] = True
+    token_of = None
+    if w.carrier_token and n_car:               # the one shifted token of each carrier page
+        token_of = np.full(n_pages, -1, dtype=np.int64)
+        token_of[carriers] = rng.integers(0, B, size=n_car)
 
     gr = w.global_rank
     H = rng.standard_normal((gr, d)) / math.sqrt(gr) if gr else None
@@ -112,7 +118,11 @@ def _gen_unit(w: LocksWorkload, b: int, h: int, seq_len: int, q_hat: np.ndarray,
             keys += (Z @ H).reshape(n, B, d)
         car = is_carrier[c0:c1]
         if car.any():
-            keys[car] += w.carrier_bias * q_hat
+            if token_of is None:
+                keys[car] += w.carrier_bias * q_hat
+            else:
+                for p in np.nonzero(car)[0]:
+                    keys[p, token_of[c0 + p]] += w.carrier_bias * q_hat
         vals = crng.standard_normal((n, B, d))
         kb = f32_to_bf16_bits(keys)
         vb = f32_to_bf16_bits(vals)
