@@ -23,6 +23,8 @@ WQ = W.get("llama32k").with_(batch=2, seed=3001)
 # the same with single-token carriers: one key of each carrier page shifted by
 # 4 along the group query direction (its page's centroid moves by 4/64)
 WP = W.get("llama32k").with_(batch=2, carrier_token=True, carrier_bias=4.0, seed=3002)
+# the paper's shipped page size: B = 16, same budget (k = 128 of 2048 pages)
+WQ16 = W.get("llama32k").with_(batch=2, page_size=16, seed=3003)
 RANKS = (2, 4, 8, 15)
 
 
@@ -134,3 +136,21 @@ def test_peaky_carriers():
     _print_table(f"\npeaky carriers (one token of each carrier page shifted by "
                  f"{w.carrier_bias}), {w.name} x{w.batch}", table)
     assert table["exact LSE (ceiling)"]["needle"] == 1.0
+
+
+def test_rank_sweep_page16():
+    """The rank sweep and the rivals at B = 16 (Table D.12's setting)."""
+    inputs = W.generate(WQ16)
+    w = inputs.workload
+    units = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
+    ex = {u: Q.unit_exact(inputs, *u) for u in units}
+    rows = {"exact LSE (ceiling)": [Q.unit_stats(ex[u], ex[u]["best"]) for u in units]}
+    _rank_sweep_and_rivals(inputs, units, ex, rows)
+    table = {name: Q.aggregate(r) for name, r in rows.items()}
+    _print_table(f"\nrank sweep at B = 16, {w.name} x{w.batch}, b = {w.budget_tokens} "
+                 f"(k = {ex[units[0]]['k']} of {ex[units[0]]['n']} pages)", table)
+    assert table["exact LSE (ceiling)"]["recall"] == 1.0
+    # a centred page of B = 16 keys has rank at most 15: at r = 15 the summary
+    # reconstructs every logit, so the GPU selection is the exact one up to
+    # float32-against-float64 rounding among near-equal shares
+    assert table["Locks r15 (fp32 record)"]["recall"] >= 0.99
