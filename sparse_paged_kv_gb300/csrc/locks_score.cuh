@@ -1,7 +1,8 @@
 // Page scoring of locks_select (Eq. (1) of "Locks: Page-Local Compact Key
 // Summaries for Efficient Long-Context Decoding", section 4 "Score"): the
-// persistent score kernel, templated on the page size B (64 or 16).  Included
-// by one translation unit per page size; internal to the library.
+// score kernel (each CTA streams one contiguous range of candidate pages),
+// templated on the page size B (64 or 16).  Included by one translation unit
+// per page size; internal to the library.
 #pragma once
 
 #include <type_traits>

@@ -5,7 +5,7 @@
 //
 // Two kernels, the second launched as a programmatic dependent of the first:
 //
-// score_kernel (persistent): the candidate pages of every (sequence b, KV
+// score_kernel: the candidate pages of every (sequence b, KV
 // head h) "unit" are laid end to end (mc slots per unit) and every CTA takes
 // one contiguous, equal range of slots.  Each of its 4 warps owns a
 // shared-memory ring of page-pair slots; lane 0 streams the summary records of

@@ -1,5 +1,7 @@
 // Selection helpers of the finalize kernel: score loads, block-wide scans and
-// the block radix top-K over a shared-memory list of share bit patterns.
+// the block top-K over a shared-memory list of share bit patterns (a lower
+// bound from the per-thread maxima, then a direct ranking of the few keys at
+// or above it; a bit-by-bit search of the K-th key when too many are).
 // Internal to the library.
 #pragma once
 
