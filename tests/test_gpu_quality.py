@@ -154,3 +154,47 @@ def test_rank_sweep_page16():
     # reconstructs every logit, so the GPU selection is the exact one up to
     # float32-against-float64 rounding among near-equal shares
     assert table["Locks r15 (fp32 record)"]["recall"] >= 0.99
+
+
+def test_log_mass_error_table():
+    """Table B.2-style measured error on the synthetic llama32k layer: per
+    candidate page and query head |s_hat - s| against the exact log-sum-exp
+    mass, and per candidate page |log m_bar_hat - log m_bar| of the
+    group-averaged shares, pooled, for the fp32, bf16 and quantised records.
+    Reported, with only finiteness checked (the error is measured, not bounded,
+    as in the paper)."""
+    import torch
+    from sparse_paged_kv_gb300 import binding as Bd, runtime
+    import oracle as O
+    inputs = W.generate(WQ)
+    w = inputs.workload
+    G, Hk = w.group, w.n_kv_heads
+    units = [(b, h) for b in range(w.batch) for h in range(Hk)]
+    ex = {u: Q.unit_exact(inputs, *u) for u in units}
+    print(f"\nmeasured log-mass error, {w.name} x{w.batch} (r = {w.rank}, B = {w.page_size})")
+    print("  record         |s_hat - s|: p50     p95     max   | group-share log error: p50     p95     max")
+    for name, dt in (("r8 fp32", Bd.LOCKS_SUMMARY_F32), ("r8 bf16", Bd.LOCKS_SUMMARY_BF16),
+                     ("r8i4", Bd.LOCKS_SUMMARY_I4)):
+        layer = runtime.LocksLayer.from_inputs(inputs, summary_dtype=dt)
+        layer.build()
+        lse, share = layer.alloc_page_lse(), layer.alloc_page_share()
+        layer.select(page_lse=lse, page_share=share)
+        torch.cuda.synchronize()
+        assert int(layer.status.cpu()[0]) == 0
+        lse, share = lse.cpu().numpy(), share.cpu().numpy()
+        e_s, e_m = [], []
+        for b, h in units:
+            x = ex[(b, h)]
+            cand = x["cand"]
+            s_hat = lse[b, h * G:(h + 1) * G][:, cand].astype(np.float64)
+            e_s.append(np.abs(s_hat - x["s"][:, cand]).ravel())
+            m_ex = O.share_average(O.page_shares(x["s"][:, cand]))
+            m_hat = share[b, h, cand].astype(np.float64)
+            e_m.append(np.abs(np.log(m_hat) - np.log(m_ex)))
+        e_s, e_m = np.concatenate(e_s), np.concatenate(e_m)
+        assert np.all(np.isfinite(e_s)) and np.all(np.isfinite(e_m))
+        print(f"  {name:14s} {np.percentile(e_s, 50):10.4f} {np.percentile(e_s, 95):7.4f} "
+              f"{e_s.max():7.3f}   {np.percentile(e_m, 50):22.4f} {np.percentile(e_m, 95):7.4f} "
+              f"{e_m.max():7.3f}")
+        del layer
+        torch.cuda.empty_cache()
