@@ -169,6 +169,25 @@ def profile_traffic(kernel_key: str, config: str):
 # --------------------------------------------------------------------------
 # replicas across ranks (weak scaling: every rank runs its own batch)
 # --------------------------------------------------------------------------
+# FP32 ALU peak: 152 SMs x 128 FP32 lanes x 2 flops per fused multiply-add x
+# 2.07 GHz (the maximum SM clock)
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def build_flop_count(sweeps, B: int, d_head: int = 128, r: int = 8) -> float:
+    """Floating-point operations the summary build executes, from the Jacobi
+    sweeps each page-head used: centring (B d), the full Gram product
+    (2 B^2 d), per sweep B-1 rounds that rotate the B x B matrix as (B/2)^2
+    2 x 2 blocks (24 flops each) and the B x B eigenvector matrix (6 flops per
+    row and pair), the convergence norms (2 B^2 per check), and the basis
+    V = D^T U_r (2 d B r)."""
+    import numpy as np
+    sweeps = np.asarray(sweeps, dtype=np.float64)
+    per_sweep = (B - 1) * (24 * (B // 2) ** 2 + 6 * B * (B // 2))
+    fixed = B * d_head + 2 * B * B * d_head + 2 * d_head * B * r
+    return float(sweeps.size * fixed + sweeps.sum() * per_sweep + (sweeps + 1).sum() * 2 * B * B)
+
+
 def captured_energy(layer, ids_t, tail, w, sample: int = 4096):
     """Energy the rank-r summary captures per page-head, 1 - tau / ||D||_F^2
     (a diagnostic the paper reports for real pages, App. D): tau is the build's
@@ -368,7 +387,9 @@ def run_gpu(args):
         build_ms.append(e0.elapsed_time(e1))
     build_ms = min(build_ms)
     page_heads = len(ids) * w.n_kv_heads
-    not_conv = int(((bstat.cpu().numpy() >> 16) != 0).sum())
+    bstat_np = bstat.cpu().numpy()
+    not_conv = int(((bstat_np >> 16) != 0).sum())
+    build_flops = build_flop_count(bstat_np & 0xFFFF, w.page_size, r=w.rank)
 
     # In a decode loop each sequence completes a page every B steps and its
     # summary is built then (off the step's critical path, section 4): time the
@@ -571,6 +592,11 @@ def run_gpu(args):
         "speedup_vs_dense": (dense["us_per_step"] / (mean_step * 1e3)) if dense else None,
         "build": {"ms": build_ms, "page_heads": page_heads, "pages_per_s": len(ids) / (build_ms / 1e3),
                   "page_heads_per_s": page_heads / (build_ms / 1e3), "not_converged": not_conv,
+                  "mean_sweeps": float((bstat_np & 0xFFFF).mean()),
+                  "roofline": {"bound": "alu", "achieved": build_flops / (build_ms / 1e3) / 1e12,
+                               "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                               "frac": build_flops / (build_ms / 1e3) / 1e12 / FP32_ALU_TFLOPS,
+                               "flops": build_flops},
                   "captured_energy": captured,
                   "page_crossing_us": crossing_us,
                   "page_crossing_per_step_us": crossing_us / w.page_size,
