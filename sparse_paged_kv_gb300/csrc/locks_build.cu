@@ -15,6 +15,7 @@
 //      coefficients); V = D^T U_r S_r^-1, C = U_r S_r,
 //      tau = sum of the remaining eigenvalues;
 //   5. the record (mu, V, C) in the layout locks_select reads.
+#include <cstddef>
 #include <type_traits>
 
 #include "locks_common.cuh"
@@ -44,17 +45,95 @@ struct BuildSmem {
   float qscale[17];             // quantised record: column scales, then the centroid's
   float tau;
   int flag;
+  unsigned char lp[PB - 1][PB / 2], lq[PB - 1][PB / 2];   // round labels (below)
 };
 
-// round k's pair t of the circle method on PB players: player PB-1 fixed, the
-// other PB-1 rotate
+// The rounds of the circle method on PB players (player PB-1 fixed, the other
+// PB-1 rotate): pair 0 of round t is (t, PB-1), pair k > 0 is (t+k, t-k) mod
+// PB-1. Which member of a pair is p and which q is free (a rotation is
+// defined for either order), and it decides the shared-memory banks of the
+// update: with a row stride of 1 mod 32, row x sits in bank x mod 32. Every
+// residue class mod 32 holds two rows and every pair two members, so one
+// member per pair can always be labelled p such that the 32 p rows (and so
+// the 32 q rows) fall in distinct banks; lanes running over a round's pairs
+// then touch 32 banks at once. The labels are found by walking the cycles
+// that pairs and residue classes form (p = the smaller member when B <= 32,
+// where all rows are in distinct banks anyway) and tabulated at compile time.
 template <int PB>
-__device__ __forceinline__ void round_pair(int t, int k, int& p, int& q) {
-  int a, b;
-  if (k == 0) { a = t; b = PB - 1; }
-  else { a = (t + k) % (PB - 1); b = (t - k + (PB - 1)) % (PB - 1); }
-  p = min(a, b);
-  q = max(a, b);
+struct alignas(16) RoundLabels {
+  unsigned char p[PB - 1][PB / 2], q[PB - 1][PB / 2];
+};
+
+template <int PB>
+constexpr RoundLabels<PB> make_round_labels() {
+  constexpr int NPR = PB / 2;
+  RoundLabels<PB> lab{};
+  for (int t = 0; t < PB - 1; ++t) {
+    int a[NPR] = {}, b[NPR] = {}, pair_of[PB] = {}, pick[NPR] = {};
+    for (int k = 0; k < NPR; ++k) {
+      a[k] = k == 0 ? t : (t + k) % (PB - 1);
+      b[k] = k == 0 ? PB - 1 : (t - k + (PB - 1)) % (PB - 1);
+      pair_of[a[k]] = k;
+      pair_of[b[k]] = k;
+      pick[k] = -1;
+    }
+    for (int k = 0; k < NPR; ++k) {
+      if (pick[k] >= 0) continue;
+      if (PB <= 32) {
+        pick[k] = a[k] < b[k] ? a[k] : b[k];
+        continue;
+      }
+      // label x as p; the other row of x's class must then be a q, so its
+      // pair's other member is a p, and so on round the cycle
+      int x = a[k], cur = k;
+      for (;;) {
+        pick[cur] = x;
+        const int y = x ^ 32;
+        const int j = pair_of[y];
+        if (pick[j] >= 0) break;
+        x = a[j] == y ? b[j] : a[j];
+        cur = j;
+      }
+    }
+    for (int k = 0; k < NPR; ++k) {
+      lab.p[t][k] = static_cast<unsigned char>(pick[k]);
+      lab.q[t][k] = static_cast<unsigned char>(pick[k] == a[k] ? b[k] : a[k]);
+    }
+  }
+  return lab;
+}
+
+// every round pairs all rows (the circle method's pairs, each once) and, at
+// B > 32, its p rows and its q rows each fall in 32 distinct banks
+template <int PB>
+constexpr bool round_labels_valid(const RoundLabels<PB>& lab) {
+  for (int t = 0; t < PB - 1; ++t) {
+    bool seen[PB] = {}, bank_p[32] = {}, bank_q[32] = {};
+    for (int k = 0; k < PB / 2; ++k) {
+      const int p = lab.p[t][k], q = lab.q[t][k];
+      if (p >= PB || q >= PB || seen[p] || seen[q] || p == q) return false;
+      seen[p] = seen[q] = true;
+      const int a = k == 0 ? t : (t + k) % (PB - 1);
+      const int b = k == 0 ? PB - 1 : (t - k + (PB - 1)) % (PB - 1);
+      if (!((p == a && q == b) || (p == b && q == a))) return false;
+      if (PB > 32) {
+        if (bank_p[p % 32] || bank_q[q % 32]) return false;
+        bank_p[p % 32] = bank_q[q % 32] = true;
+      }
+    }
+  }
+  return true;
+}
+static_assert(round_labels_valid<64>(make_round_labels<64>()), "round labels (B = 64)");
+static_assert(round_labels_valid<16>(make_round_labels<16>()), "round labels (B = 16)");
+
+__device__ const RoundLabels<64> kRoundLabels64 = make_round_labels<64>();
+__device__ const RoundLabels<16> kRoundLabels16 = make_round_labels<16>();
+
+template <int PB>
+__device__ __forceinline__ const RoundLabels<PB>& round_labels() {
+  if constexpr (PB == 64) return kRoundLabels64;
+  else return kRoundLabels16;
 }
 
 // Quantised record (section 4 "Build": int4 basis with one scale per column,
@@ -240,6 +319,14 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     const int i = idx / PB, j = idx % PB;
     S.U[i * kAS + j] = (i == j) ? 1.f : 0.f;
   }
+  {
+    static_assert(sizeof(RoundLabels<PB>) % 4 == 0 && offsetof(BuildSmem<PB>, lp) % 4 == 0 &&
+                      offsetof(BuildSmem<PB>, lq) == offsetof(BuildSmem<PB>, lp) + sizeof(S.lp),
+                  "round labels are copied as words");
+    const uint32_t* src_l = reinterpret_cast<const uint32_t*>(&round_labels<PB>());
+    uint32_t* dst_l = reinterpret_cast<uint32_t*>(&S.lp[0][0]);
+    for (int w = tid; w < int(sizeof(RoundLabels<PB>) / 4); w += kBuildThreads) dst_l[w] = src_l[w];
+  }
   __syncthreads();
 
   // ---- 3. Jacobi sweeps ------------------------------------------------------
@@ -269,8 +356,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     ++sweeps;
     for (int r = 0; r < PB - 1; ++r) {
       if (tid < NPR) {
-        int p, q;
-        round_pair<PB>(r, tid, p, q);
+        const int p = S.lp[r][tid], q = S.lq[r][tid];
         const float app = S.A[p * kAS + p], aqq = S.A[q * kAS + q], apq = S.A[p * kAS + q];
         float c = 1.f, s = 0.f;
         if (apq != 0.f) {
@@ -285,14 +371,16 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
       }
       __syncthreads();
       if (NPR * NPR >= kBuildThreads || tid < NPR * NPR) {
-        // 2 x 2 blocks (K, L): rows (pK, qK), cols (pL, qL); B'' = J_K^T B J_L
-        // (B = 64: thread owns K = tid / 8 and L = tid % 8 + 8m; B = 16: one block)
-        const int K = tid >> 3;
+        // 2 x 2 blocks (K, L): rows (pK, qK), cols (pL, qL); B'' = J_K^T B J_L.
+        // Block tid + 256 m is K = tid % NPR, L = (tid + 256 m) / NPR: the
+        // lanes of a warp run over the pairs K, one column pair L per warp.
+        static_assert(kBuildThreads % NPR == 0, "K is fixed per thread");
+        const int K = tid % NPR;
         const float cK = S.rot_c[K], sK = S.rot_s[K];
         const int pK = S.rot_p[K], qK = S.rot_q[K];
 #pragma unroll
         for (int m = 0; m < (NPR * NPR + kBuildThreads - 1) / kBuildThreads; ++m) {
-          const int L = (tid & 7) + 8 * m;
+          const int L = (tid + kBuildThreads * m) / NPR;
           const float cL = S.rot_c[L], sL = S.rot_s[L];
           const int pL = S.rot_p[L], qL = S.rot_q[L];
           float* a00 = S.A + pK * kAS + pL;
@@ -308,15 +396,15 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
           *a00 = n00; *a01 = n01; *a10 = n10; *a11 = n11;
         }
       }
-      // U <- U J: pair L = tid % NPR, rows tid / NPR + (256 / NPR) m
+      // U <- U J: item tid + 256 m is row i = item % B of pair L = item / B
+      // (the lanes of a warp run over consecutive rows)
       if (NPR * PB >= kBuildThreads || tid < NPR * PB) {
-        const int L = tid % NPR;
-        const float cL = S.rot_c[L], sL = S.rot_s[L];
-        const int pL = S.rot_p[L], qL = S.rot_q[L];
-        constexpr int RS = kBuildThreads / NPR;       // row step
 #pragma unroll
-        for (int m = 0; m < (PB + RS - 1) / RS; ++m) {
-          const int i = tid / NPR + RS * m;
+        for (int m = 0; m < (NPR * PB + kBuildThreads - 1) / kBuildThreads; ++m) {
+          const int it = tid + kBuildThreads * m;
+          const int i = it % PB, L = it / PB;
+          const float cL = S.rot_c[L], sL = S.rot_s[L];
+          const int pL = S.rot_p[L], qL = S.rot_q[L];
           const float up = S.U[i * kAS + pL], uq = S.U[i * kAS + qL];
           S.U[i * kAS + pL] = up * cL - uq * sL;
           S.U[i * kAS + qL] = up * sL + uq * cL;
