@@ -37,8 +37,7 @@ struct BuildSmem {
   float A[PB * AS];
   float U[PB * AS];
   float mu[kHeadDim];
-  float rot_c[PB / 2], rot_s[PB / 2];
-  int rot_p[PB / 2], rot_q[PB / 2];
+  float4 rot[PB / 2];           // the round's rotations: c, s and the rows p, q (as bits)
   float red[kBuildThreads / 32 * 2];
   float lam[16];
   int order[16];
@@ -367,7 +366,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
           c = rsqrtf(1.f + t * t);
           s = t * c;
         }
-        S.rot_c[tid] = c; S.rot_s[tid] = s; S.rot_p[tid] = p; S.rot_q[tid] = q;
+        S.rot[tid] = make_float4(c, s, __int_as_float(p), __int_as_float(q));
       }
       __syncthreads();
       if (NPR * NPR >= kBuildThreads || tid < NPR * NPR) {
@@ -376,13 +375,15 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
         // lanes of a warp run over the pairs K, one column pair L per warp.
         static_assert(kBuildThreads % NPR == 0, "K is fixed per thread");
         const int K = tid % NPR;
-        const float cK = S.rot_c[K], sK = S.rot_s[K];
-        const int pK = S.rot_p[K], qK = S.rot_q[K];
+        const float4 rK = S.rot[K];
+        const float cK = rK.x, sK = rK.y;
+        const int pK = __float_as_int(rK.z), qK = __float_as_int(rK.w);
 #pragma unroll
         for (int m = 0; m < (NPR * NPR + kBuildThreads - 1) / kBuildThreads; ++m) {
           const int L = (tid + kBuildThreads * m) / NPR;
-          const float cL = S.rot_c[L], sL = S.rot_s[L];
-          const int pL = S.rot_p[L], qL = S.rot_q[L];
+          const float4 rL = S.rot[L];                 // one broadcast load per warp
+          const float cL = rL.x, sL = rL.y;
+          const int pL = __float_as_int(rL.z), qL = __float_as_int(rL.w);
           float* a00 = S.A + pK * kAS + pL;
           float* a01 = S.A + pK * kAS + qL;
           float* a10 = S.A + qK * kAS + pL;
@@ -403,8 +404,9 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
         for (int m = 0; m < (NPR * PB + kBuildThreads - 1) / kBuildThreads; ++m) {
           const int it = tid + kBuildThreads * m;
           const int i = it % PB, L = it / PB;
-          const float cL = S.rot_c[L], sL = S.rot_s[L];
-          const int pL = S.rot_p[L], qL = S.rot_q[L];
+          const float4 rL = S.rot[L];
+          const float cL = rL.x, sL = rL.y;
+          const int pL = __float_as_int(rL.z), qL = __float_as_int(rL.w);
           const float up = S.U[i * kAS + pL], uq = S.U[i * kAS + qL];
           S.U[i * kAS + pL] = up * cL - uq * sL;
           S.U[i * kAS + qL] = up * sL + uq * cL;
