@@ -33,9 +33,14 @@ constexpr float kDropRel = 1e-5f;
 template <int PB>
 struct BuildSmem {
   static constexpr int AS = PB + 1;   // padded row stride of A and U
-  float D[PB * kDS];
-  float A[PB * AS];
-  float U[PB * AS];
+  // D (the centred keys) is dead once the Gram sits in registers: A and U
+  // reuse its space, and so does the quantised record's scratch (basis values
+  // [16][d], then coefficient scales [B]), inside the dead A where it fits
+  static constexpr int kScratch = 16 * kHeadDim + PB;
+  static constexpr bool kScratchInA = PB * AS >= kScratch;
+  static constexpr int kWorkD = PB * kDS;
+  static constexpr int kWorkJ = 2 * PB * AS + (kScratchInA ? 0 : kScratch);
+  float work[kWorkD > kWorkJ ? kWorkD : kWorkJ];
   float mu[kHeadDim];
   float4 rot[PB / 2];           // the round's rotations: c, s and the rows p, q (as bits)
   float red[kBuildThreads / 32 * 2];
@@ -45,6 +50,12 @@ struct BuildSmem {
   float tau;
   int flag;
   unsigned char lp[PB - 1][PB / 2], lq[PB - 1][PB / 2];   // round labels (below)
+
+  __device__ float* D() { return work; }             // [B][kDS]: steps 1-2
+  __device__ float* A() { return work; }             // [B][AS]: steps 2-4
+  __device__ float* U() { return work + PB * AS; }   // [B][AS]: steps 2-5
+  __device__ float* Vs() { return work + (kScratchInA ? 0 : 2 * PB * AS); }   // step 5
+  __device__ float* cs() { return Vs() + 16 * kHeadDim; }                       // step 5
 };
 
 // The rounds of the circle method on PB players (player PB-1 fixed, the other
@@ -153,20 +164,25 @@ __device__ __forceinline__ void write_i4_record(Smem& S, const BuildParams& prm,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned char* rb = static_cast<unsigned char*>(prm.summaries) +
                       (size_t(blk) * prm.n_kv_heads + h) * prm.rec_bytes;
-  // basis values v_k[t] (as the float record stores them) into the idle D array
+  const float* U = S.U();
+  // basis values v_k[t] (as the float record stores them), D re-formed from
+  // the key page as step 1 formed it
   float v[RP];
   if (tid < kHeadDim) {
+    const __nv_bfloat16* kp = prm.k_cache + (size_t(blk) * prm.n_kv_heads + h) * (PB * kHeadDim);
+    const float mu_t = S.mu[tid];
 #pragma unroll
     for (int k = 0; k < RP; ++k) v[k] = 0.f;
+#pragma unroll 8
     for (int i = 0; i < PB; ++i) {
-      const float dit = S.D[i * kDS + tid];
+      const float dit = __bfloat162float(kp[i * kHeadDim + tid]) - mu_t;
 #pragma unroll
       for (int k = 0; k < RP; ++k)
-        if (k < r) v[k] += dit * S.U[i * kAS + S.order[k]];
+        if (k < r) v[k] += dit * U[i * kAS + S.order[k]];
     }
   }
   __syncthreads();
-  float* Vs = S.D;                                         // [RP][d]
+  float* Vs = S.Vs();                                      // [RP][d]
   if (tid < kHeadDim) {
 #pragma unroll
     for (int k = 0; k < RP; ++k) {
@@ -222,10 +238,10 @@ __device__ __forceinline__ void write_i4_record(Smem& S, const BuildParams& prm,
   }
   // coefficient rows: their scales first (one per token), then the codes in
   // the scorer's fragment order
-  float* cs = S.A;                                           // [PB] (A is idle now)
+  float* cs = S.cs();                                        // [PB]
   auto coeff = [&](int i, int k) {
     const float lam = k < r ? S.lam[k] : 0.f;
-    return lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
+    return lam > 0.f ? U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
   };
   if (tid < PB) {
     float am = 0.f;
@@ -253,6 +269,9 @@ template <int RP, typename T, int PB>
 __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams prm) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BuildSmem<PB>& S = *reinterpret_cast<BuildSmem<PB>*>(smem_raw);
+  float* const D = S.D();
+  float* const A = S.A();
+  float* const U = S.U();
   constexpr int kAS = BuildSmem<PB>::AS;
   constexpr int NPR = PB / 2;          // rotations per round
   constexpr int TT = PB / 16;          // Gram register tile edge
@@ -274,20 +293,20 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     const int idx = tid + kBuildThreads * e;       // 16-byte chunk of the 16 KiB page
     const int row = idx >> 4, col = (idx & 15) * 8;
     const uint4 w = src[idx];
-    float* d = S.D + row * kDS + col;
+    float* d = D + row * kDS + col;
     d[0] = bf16_lo(w.x); d[1] = bf16_hi(w.x); d[2] = bf16_lo(w.y); d[3] = bf16_hi(w.y);
     d[4] = bf16_lo(w.z); d[5] = bf16_hi(w.z); d[6] = bf16_lo(w.w); d[7] = bf16_hi(w.w);
   }
   __syncthreads();
   if (tid < kHeadDim) {
     float s = 0.f;
-    for (int i = 0; i < PB; ++i) s += S.D[i * kDS + tid];
+    for (int i = 0; i < PB; ++i) s += D[i * kDS + tid];
     S.mu[tid] = s * (1.f / PB);
   }
   __syncthreads();
   for (int idx = tid; idx < PB * kHeadDim; idx += kBuildThreads) {
     const int i = idx >> 7, t = idx & 127;
-    S.D[i * kDS + t] -= S.mu[t];
+    D[i * kDS + t] -= S.mu[t];
   }
   __syncthreads();
 
@@ -299,8 +318,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
       float4 di[TT], dj[TT];
 #pragma unroll
       for (int a = 0; a < TT; ++a) {
-        di[a] = *reinterpret_cast<const float4*>(S.D + (ti + 16 * a) * kDS + c);
-        dj[a] = *reinterpret_cast<const float4*>(S.D + (tj + 16 * a) * kDS + c);
+        di[a] = *reinterpret_cast<const float4*>(D + (ti + 16 * a) * kDS + c);
+        dj[a] = *reinterpret_cast<const float4*>(D + (tj + 16 * a) * kDS + c);
       }
 #pragma unroll
       for (int a = 0; a < TT; ++a)
@@ -309,14 +328,15 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
           acc[a][bb] += di[a].x * dj[bb].x + di[a].y * dj[bb].y + di[a].z * dj[bb].z +
                         di[a].w * dj[bb].w;
     }
+    __syncthreads();   // every read of D is done: A and U overwrite it
 #pragma unroll
     for (int a = 0; a < TT; ++a)
 #pragma unroll
-      for (int bb = 0; bb < TT; ++bb) S.A[(ti + 16 * a) * kAS + tj + 16 * bb] = acc[a][bb];
+      for (int bb = 0; bb < TT; ++bb) A[(ti + 16 * a) * kAS + tj + 16 * bb] = acc[a][bb];
   }
   for (int idx = tid; idx < PB * PB; idx += kBuildThreads) {
     const int i = idx / PB, j = idx % PB;
-    S.U[i * kAS + j] = (i == j) ? 1.f : 0.f;
+    U[i * kAS + j] = (i == j) ? 1.f : 0.f;
   }
   {
     static_assert(sizeof(RoundLabels<PB>) % 4 == 0 && offsetof(BuildSmem<PB>, lp) % 4 == 0 &&
@@ -336,7 +356,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     float off = 0.f, tot = 0.f;
     for (int idx = tid; idx < PB * PB; idx += kBuildThreads) {
       const int i = idx / PB, j = idx % PB;
-      const float a = S.A[i * kAS + j];
+      const float a = A[i * kAS + j];
       tot += a * a;
       if (i != j) off += a * a;
     }
@@ -356,7 +376,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     for (int r = 0; r < PB - 1; ++r) {
       if (tid < NPR) {
         const int p = S.lp[r][tid], q = S.lq[r][tid];
-        const float app = S.A[p * kAS + p], aqq = S.A[q * kAS + q], apq = S.A[p * kAS + q];
+        const float app = A[p * kAS + p], aqq = A[q * kAS + q], apq = A[p * kAS + q];
         float c = 1.f, s = 0.f;
         if (apq != 0.f) {
           const float theta = (aqq - app) / (2.f * apq);
@@ -384,10 +404,10 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
           const float4 rL = S.rot[L];                 // one broadcast load per warp
           const float cL = rL.x, sL = rL.y;
           const int pL = __float_as_int(rL.z), qL = __float_as_int(rL.w);
-          float* a00 = S.A + pK * kAS + pL;
-          float* a01 = S.A + pK * kAS + qL;
-          float* a10 = S.A + qK * kAS + pL;
-          float* a11 = S.A + qK * kAS + qL;
+          float* a00 = A + pK * kAS + pL;
+          float* a01 = A + pK * kAS + qL;
+          float* a10 = A + qK * kAS + pL;
+          float* a11 = A + qK * kAS + qL;
           const float b00 = *a00, b01 = *a01, b10 = *a10, b11 = *a11;
           const float x00 = cK * b00 - sK * b10, x01 = cK * b01 - sK * b11;
           const float x10 = sK * b00 + cK * b10, x11 = sK * b01 + cK * b11;
@@ -407,9 +427,9 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
           const float4 rL = S.rot[L];
           const float cL = rL.x, sL = rL.y;
           const int pL = __float_as_int(rL.z), qL = __float_as_int(rL.w);
-          const float up = S.U[i * kAS + pL], uq = S.U[i * kAS + qL];
-          S.U[i * kAS + pL] = up * cL - uq * sL;
-          S.U[i * kAS + qL] = up * sL + uq * cL;
+          const float up = U[i * kAS + pL], uq = U[i * kAS + qL];
+          U[i * kAS + pL] = up * cL - uq * sL;
+          U[i * kAS + qL] = up * sL + uq * cL;
         }
       }
       __syncthreads();
@@ -420,8 +440,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   const int r = prm.rank;
   if (warp == 0) {
     // lane holds diagonal entries lane and lane + 32 (those past B count as taken)
-    float v0 = lane < PB ? S.A[lane * kAS + lane] : 0.f;
-    float v1 = lane + 32 < PB ? S.A[(lane + 32) * kAS + lane + 32] : 0.f;
+    float v0 = lane < PB ? A[lane * kAS + lane] : 0.f;
+    float v1 = lane + 32 < PB ? A[(lane + 32) * kAS + lane + 32] : 0.f;
     bool t0 = lane >= PB, t1 = lane + 32 >= PB;
     float lam1 = 0.f;
     for (int k = 0; k < r; ++k) {
@@ -459,15 +479,19 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
                                   (size_t(blk) * prm.n_kv_heads + h) * prm.rec_bytes);
     if (tid < kHeadDim) {
       const int t = tid;
-      st_elem(rec + t, S.mu[t]);
+      const float mu_t = S.mu[t];
+      st_elem(rec + t, mu_t);
+      // D re-formed from the key page as step 1 formed it (A and U hold its space)
+      const __nv_bfloat16* kp = prm.k_cache + (size_t(blk) * prm.n_kv_heads + h) * (PB * kHeadDim);
       float v[RP];
 #pragma unroll
       for (int k = 0; k < RP; ++k) v[k] = 0.f;
+#pragma unroll 8
       for (int i = 0; i < PB; ++i) {
-        const float dit = S.D[i * kDS + t];
+        const float dit = __bfloat162float(kp[i * kHeadDim + t]) - mu_t;
 #pragma unroll
         for (int k = 0; k < RP; ++k)
-          if (k < r) v[k] += dit * S.U[i * kAS + S.order[k]];
+          if (k < r) v[k] += dit * U[i * kAS + S.order[k]];
       }
 #pragma unroll
       for (int k = 0; k < RP; ++k) {
@@ -479,7 +503,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
       for (int idx = tid - kHeadDim; idx < PB * RP; idx += kBuildThreads - kHeadDim) {
         const int i = idx / RP, k = idx % RP;
         const float lam = k < r ? S.lam[k] : 0.f;
-        const float c = lam > 0.f ? S.U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
+        const float c = lam > 0.f ? U[i * kAS + S.order[k]] * sqrtf(lam) : 0.f;
         st_elem(C + ((k >> 2) * PB + i) * 4 + (k & 3), c);
       }
     }
