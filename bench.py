@@ -167,7 +167,7 @@ def profile_traffic(kernel_key: str, config: str):
 
 
 # --------------------------------------------------------------------------
-# replicas across ranks (weak scaling: every rank runs its own batch)
+# summary build diagnostics
 # --------------------------------------------------------------------------
 # FP32 ALU peak: 152 SMs x 128 FP32 lanes x 2 flops per fused multiply-add x
 # 2.07 GHz (the maximum SM clock)
@@ -208,6 +208,9 @@ def captured_energy(layer, ids_t, tail, w, sample: int = 4096):
             "p10": float(q[0]), "p90": float(q[2]), "mean": float(frac.mean())}
 
 
+# --------------------------------------------------------------------------
+# replicas across ranks (weak scaling: every rank runs its own batch)
+# --------------------------------------------------------------------------
 def replica_workload(w, rank: int):
     """Rank r's replica of workload w: same shapes, its own seed."""
     return w.with_(seed=w.seed + 7919 * rank) if rank else w
