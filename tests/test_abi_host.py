@@ -100,6 +100,36 @@ def test_select_validation(lib):
                             None, None) == B.LOCKS_ERR_INVALID_ARG
 
 
+def test_supported_shape_limits(lib):
+    """The header's shape limits: G a power of two up to 8, page ids below
+    2^24, record indices below 2^31; a negative batch is invalid."""
+    assert _select(lib, cfg(n_q_heads=12, n_kv_heads=4)) == B.LOCKS_ERR_UNSUPPORTED   # G = 3
+    assert _select(lib, cfg(n_q_heads=32, n_kv_heads=2)) == B.LOCKS_ERR_UNSUPPORTED   # G = 16
+    assert _select(lib, cfg(max_pages=1 << 24)) == B.LOCKS_ERR_UNSUPPORTED
+    assert _select(lib, cfg(num_blocks=1 << 30, n_kv_heads=2)) == B.LOCKS_ERR_UNSUPPORTED
+    assert _select(lib, cfg(batch=-1)) == B.LOCKS_ERR_INVALID_ARG
+    for c in (cfg(max_pages=1 << 24), cfg(n_q_heads=12, n_kv_heads=4), cfg(batch=-1)):
+        assert lib.locks_summary_record_bytes(ctypes.byref(c.c())) == 0
+        assert lib.locks_select_workspace_bytes(ctypes.byref(c.c()), 512) == 0
+        assert lib.locks_decode_workspace_bytes(ctypes.byref(c.c()), 8) == 0
+    # just inside the limits
+    assert lib.locks_summary_record_bytes(ctypes.byref(cfg(max_pages=(1 << 24) - 1).c())) > 0
+    assert lib.locks_summary_record_bytes(ctypes.byref(cfg(n_q_heads=16, n_kv_heads=2).c())) > 0
+
+
+def test_decode_rejects_unaligned_pools(lib):
+    """The decode reads K and V through tensor maps, whose base must be
+    16-byte aligned; a misaligned pool is refused before any launch."""
+    c = cfg()
+    ws = B.decode_workspace_bytes(c, 8)
+    odd = FAKE + 8
+    assert lib.locks_sparse_decode(ctypes.byref(c.c()), FAKE, odd, FAKE, FAKE, FAKE, FAKE, 8,
+                                   FAKE, None, FAKE, ws, None, None) == B.LOCKS_ERR_INVALID_ARG
+    assert lib.locks_dense_decode(ctypes.byref(c.c()), FAKE, FAKE, odd, FAKE, FAKE, FAKE, None,
+                                  FAKE, B.decode_workspace_bytes(c, c.max_pages), None,
+                                  None) == B.LOCKS_ERR_INVALID_ARG
+
+
 def test_decode_and_build_validation(lib):
     c = cfg()
     ws = B.decode_workspace_bytes(c, 8)
