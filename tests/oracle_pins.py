@@ -423,12 +423,74 @@ def pin_quantized_summary_groups(O):
     assert np.all(np.abs(d.mu - mu) <= float(q.mu_scale) * 0.5 + 1e-7)
 
 
+def pin_unit_driver(O):
+    """The whole-unit drivers follow the stated conventions (section 2; section
+    4 "Build"): query head g uses KV head g // G (contiguous groups), the page
+    budget is k = ceil(b / B) pages, and only complete pages get a summary
+    ("once, when a page completes").  The other groups' queries and every slot
+    past a sequence's last token are NaN, so a driver that reads them gives a
+    NaN result; sparse and dense outputs are checked against attention over
+    the contiguous arrays the cache was filled from."""
+    rng = _rng(37)
+    B, d, Hk, G, r = 16, 128, 2, 2, 4
+    Hq = Hk * G
+    T = 5 * B + 7                     # five complete pages and a partial tail
+    n = -(-T // B)
+    nb = n + 2
+    K = rng.standard_normal((Hk, T, d))
+    Vv = rng.standard_normal((Hk, T, d))
+    K[:, 3 * B:4 * B] += 1.0          # one page that should win the selection
+
+    def bits(x):
+        u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+    perm = rng.permutation(nb)
+    k_cache = np.full((nb, Hk, B, d), 0x7FC0, dtype=np.uint16)
+    v_cache = np.full((nb, Hk, B, d), 0x7FC0, dtype=np.uint16)
+    Kb, Vb = bits(K), bits(Vv)
+    for j in range(n):
+        nv = min(B, T - j * B)
+        k_cache[perm[j], :, :nv] = Kb[:, j * B:j * B + nv]
+        v_cache[perm[j], :, :nv] = Vb[:, j * B:j * B + nv]
+    bt = np.full((1, n + 1), -1, dtype=np.int32)
+    bt[0, :n] = perm[:n]
+    seq = np.array([T], dtype=np.int32)
+    budget = 3 * B + 1                # k = ceil(49 / 16) = 4, floor would give 3
+    for h in range(Hk):
+        qf = rng.standard_normal((Hq, d))
+        qf[np.arange(Hq) // G != h] = np.nan          # other groups' queries
+        q_bits = bits(qf)[None]
+        res = O.run_unit(q_bits, k_cache, v_cache, bt, seq, Hk, r, budget, 0, h, dense=True)
+        # complete pages only: pages 0..4 summarised, the partial tail is not
+        assert sorted(res.summaries) == list(range(n - 1)), sorted(res.summaries)
+        for s in res.summaries.values():
+            assert np.all(np.isfinite(s.V)) and np.all(np.isfinite(s.C))
+        # k = ceil(b / B) pages, the forced pair inside
+        sel = [int(j) for j in res.sel.selected]
+        assert len(sel) == 4 and sel[0] == 0 and sel[-1] == n - 1, sel
+        # the group's own queries, against the contiguous arrays
+        q_own = O.bf16_to_f64(q_bits[0, h * G:(h + 1) * G])
+        Kf, Vf = O.bf16_to_f64(Kb[h]), O.bf16_to_f64(Vb[h])
+        o2, l2 = O.attend(q_own, Kf, Vf)
+        assert np.all(np.isfinite(res.o_dense))
+        assert np.allclose(res.o_dense, o2, atol=1e-12) and np.allclose(res.lse_dense, l2, atol=1e-12)
+        idx = np.concatenate([np.arange(j * B, min(T, (j + 1) * B)) for j in sel])
+        o3, l3 = O.attend(q_own, Kf[idx], Vf[idx])
+        assert np.allclose(res.o_sparse, o3, atol=1e-12) and np.allclose(res.lse_sparse, l3, atol=1e-12)
+    # a length that is a multiple of B: the last page is complete and summarised
+    res = O.run_unit(q_bits, k_cache, v_cache, bt, np.array([5 * B], dtype=np.int32), Hk, r,
+                     budget, 0, Hk - 1)
+    assert sorted(res.summaries) == list(range(5))
+
+
 ALL_PINS = [
     pin_worked_example, pin_isotropic_null, pin_exact_rank, pin_full_rank_r15,
     pin_svd_route, pin_centroid_closed_form, pin_prop2, pin_lemma3,
     pin_shares_and_sandwich, pin_budget_rule, pin_forced_pages, pin_select_bruteforce,
     pin_exact_rank_selection_and_retention, pin_attention, pin_paged_attention,
     pin_quantizer_example, pin_quantizer_bounds, pin_quantized_summary_groups,
+    pin_unit_driver,
 ]
 # the cheap ones, for the planted-mistake runs
 FAST_PINS = [p for p in ALL_PINS if p is not pin_isotropic_null]

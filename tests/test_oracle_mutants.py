@@ -42,6 +42,10 @@ MUTANTS = {
                               "quantize_symmetric(V, INT4_QMAX)[1])"),
     "quant_basis_int8": ("v_codes[:, k], v_scales[k] = quantize_symmetric(V[:, k], INT4_QMAX)",
                          "v_codes[:, k], v_scales[k] = quantize_symmetric(V[:, k], INT8_QMAX)"),
+    "unit_queries_interleaved": ("q = bf16_to_f64(q_bits[b, h * G:(h + 1) * G])",
+                                 "q = bf16_to_f64(q_bits[b, h::n_kv_heads])"),
+    "unit_budget_floor": ("k = page_budget(budget_tokens, B)", "k = budget_tokens // B"),
+    "build_partial_tail": ("n_complete = seq_len // B", "n_complete = -(-seq_len // B)"),
 }
 
 
