@@ -242,9 +242,10 @@ int locks_dense_decode(const locks_cfg_t* cfg, const void* q, const void* k_cach
  * Shapes whose locks_select_workspace_bytes(cfg, budget_tokens) exceeds
  * LOCKS_SELECT_NOALLOC_MAX_BYTES are rejected with LOCKS_ERR_WORKSPACE (for
  * example, with G = 4, batch x n_kv_heads x max_pages must stay below about
- * 250,000 pages).  The first call on a device, with that device current,
- * looks up the array's device address; make that first call before any stream
- * capture.  Every call clears the scratch it uses on `stream` before selecting.
+ * 250,000 pages).  The array's device address is looked up by the first call
+ * on a device (with that device current) and again by the first call after
+ * that device's context was destroyed and re-created (cudaDeviceReset): make
+ * those calls before any stream capture.  Every call clears the scratch it uses on `stream` before selecting.
  * All calls share the one array: calls that can overlap on the GPU race.
  */
 #define LOCKS_SELECT_NOALLOC_MAX_BYTES (4u << 20)

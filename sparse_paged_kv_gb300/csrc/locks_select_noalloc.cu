@@ -11,8 +11,10 @@
 //
 // The array costs LOCKS_SELECT_NOALLOC_MAX_BYTES of device memory on every GPU
 // that loads the library, held until the process exits.  Its device address is
-// looked up once per device, on the first call made while that device is
-// current; that first call should therefore come before any stream capture.
+// looked up once per device context: on the first call made while that device
+// is current, and again on the first call after the context was destroyed and
+// created anew (cudaDeviceReset reloads the library's module, which can move
+// the array).  Those calls should therefore come before any stream capture.
 // Every call clears the part of the array it uses (an asynchronous memset on
 // the caller's stream) and then runs the same selection kernel as
 // locks_select.  All calls share the one array: calls that may overlap on the
@@ -29,20 +31,57 @@ static __device__ __align__(256) unsigned char g_select_scratch[LOCKS_SELECT_NOA
 
 constexpr int kMaxDevices = 256;
 std::mutex g_scratch_mu;
-std::array<void*, kMaxDevices> g_scratch_ptr{};   // device address per device ordinal
+struct ScratchSlot {
+  unsigned long long ctx_id;   // cuCtxGetId of the context the address belongs to
+  void* ptr;                   // device address of g_select_scratch in that context
+};
+std::array<ScratchSlot, kMaxDevices> g_scratch{};   // per device ordinal
 
-// Device address of the scratch array on the current device (looked up once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The id of the calling thread's current context (unique within the process
+// and never reused, unlike the context handle); false when no context is
+// current or the driver does not offer the calls.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current device's context, looked
+// up again whenever that context is not the one the cached address came from.
 int scratch_on_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LOCKS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
+  ScratchSlot& slot = g_scratch[dev];
+  unsigned long long id = 0;
+  if (slot.ptr == nullptr || !current_context_id(&id) || id != slot.ctx_id) {
+    void* p = nullptr;   // the lookup also makes the device's primary context current
     if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || p == nullptr)
       return LOCKS_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    if (!current_context_id(&id)) return LOCKS_ERR_CUDA;
+    slot.ctx_id = id;
+    slot.ptr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = slot.ptr;
   return LOCKS_OK;
 }
 
