@@ -7,7 +7,14 @@ locks_sparse_decode (attention over the selected pages).  Summaries are built
 once before timing (their build rate is reported separately), and the dense
 full-cache decode kernel is timed on the same inputs as the comparison point.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl locks|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config all|NAME]
+                  [--summary f32|bf16|i4] [--extra-summary i4,...] [--impl locks|reference]
+
+With the default ``--config all`` every workload is measured in one process
+(tiny, llama32k, long128k, qwen16k, 1m); the headline numbers of the JSON line
+are those of the largest, 1m (Llama-3.1-8B layer shape, batch 1, 1,048,576
+tokens), and ``per_config`` holds every workload's step, select and decode
+times, HBM fractions, the dense kernel and the CPU oracle beside them.
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own
 replica batch (weak scaling, no collective on the data path); value is the
@@ -16,6 +23,7 @@ tokens of all ranks divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -30,25 +38,37 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-step µs and tokens/s at 1 GB300 (sparse vs dense); achieved HBM GB/s vs peak"
-DEFAULT_CONFIG = "llama32k"
+HEADLINE_CONFIG = "1m"
+ALL_CONFIGS = ("tiny", "llama32k", "long128k", "qwen16k", "1m")
 FALLBACK_HBM_GBS = 6800.0
+# kernels one sparse step launches: score, finalize (select) and decode
+LAUNCHES_PER_STEP = 3
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("locks", "reference"), default="locks")
-    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--config", default="all",
+                    help="'all' (every workload, 1m as the headline) or one workload name")
     ap.add_argument("--summary", choices=("f32", "bf16", "i4"), default="f32",
-                    help="summary record: fp32, bf16, or quantised (int4 basis, int8 "
-                         "coefficients and centroid)")
+                    help="summary record of the headline step: fp32, bf16, or quantised "
+                         "(int4 basis, int8 coefficients and centroid)")
+    ap.add_argument("--extra-summary", default="i4",
+                    help="comma-separated record types also measured per workload ('' for none)")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
+
+
+def config_list(arg: str):
+    if arg == "all":
+        return list(ALL_CONFIGS), HEADLINE_CONFIG
+    return [arg], arg
 
 
 # --------------------------------------------------------------------------
@@ -64,73 +84,101 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled in the background."""
+    """SM clock and clock-event (throttle) reasons of one GPU, read through
+    NVML by a background thread every half millisecond while a region runs,
+    plus one reading at each end of the region.  Reading only: nothing is
+    set.  Without NVML the sampler reports nothing."""
 
-    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_CLOCK_SM = 1
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int, interval_ms: int = 50):
-        self.index = index
-        self.interval_ms = interval_ms
-        self.proc = None
-        self.lines = []
-        self.t0 = self.t1 = None
-
-    def start(self):
+    def __init__(self, cuda_index: int, interval_s: float = 0.0005):
+        self.interval_s = interval_s
+        self.lib = None
+        self.handle = ctypes.c_void_p()
+        self.samples = {}            # region name -> [(sm_mhz, reasons mask)]
+        self.max_mhz = None
+        self.error = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", f"-lms", str(self.interval_ms)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, ValueError):
-            self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            if not self._handle(lib, cuda_index):
+                raise OSError("no NVML handle for the CUDA device")
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(self.handle, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.lib = lib
+        except (OSError, AttributeError) as exc:
+            self.error = str(exc)[:200]
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
-
-    def mark_begin(self):
-        self.t0 = time.time()
-
-    def mark_end(self):
-        self.t1 = time.time()
-
-    def stop(self):
-        if self.proc is None:
-            return None
-        time.sleep(self.interval_ms / 1000.0 * 1.5)
-        self.proc.terminate()
+    def _handle(self, lib, cuda_index: int) -> bool:
         try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=2)
-        rows = []
-        for t, line in self.lines:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                rows.append((t, float(parts[2]), float(parts[3]), parts[5:]))
-            except ValueError:
-                continue
-        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or r[0])]
-        use = inside or rows
-        if not use:
+            import torch
+            p = torch.cuda.get_device_properties(cuda_index)
+            bus = "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle)) == 0:
+                return True
+        except (AttributeError, RuntimeError):
+            pass
+        return lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.handle)) == 0
+
+    def read(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, ctypes.byref(clk)) != 0:
             return None
-        reasons = set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for r in use:
-            for name, v in zip(names, r[3][1:5]):
-                if v.strip().lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
-                "reasons": sorted(reasons), "samples": len(use),
-                "window": "timed region" if inside else "whole run (no sample inside the timed region)"}
+        if self.reason_fn(self.handle, ctypes.byref(rs)) != 0:
+            return None
+        return float(clk.value), int(rs.value)
+
+    class _Region:
+        def __init__(self, sampler, name):
+            self.s, self.name, self.stop = sampler, name, threading.Event()
+
+        def _loop(self):
+            out = self.s.samples.setdefault(self.name, [])
+            while not self.stop.is_set():
+                r = self.s.read()
+                if r:
+                    out.append(r)
+                time.sleep(self.s.interval_s)
+
+        def __enter__(self):
+            if self.s.lib is None:
+                return self
+            r = self.s.read()
+            if r:
+                self.s.samples.setdefault(self.name, []).append(r)
+            self.t = threading.Thread(target=self._loop, daemon=True)
+            self.t.start()
+            return self
+
+        def __exit__(self, *exc):
+            if self.s.lib is None:
+                return False
+            self.stop.set()
+            self.t.join(timeout=2)
+            r = self.s.read()
+            if r:
+                self.s.samples.setdefault(self.name, []).append(r)
+            return False
+
+    def region(self, name: str):
+        return self._Region(self, name)
+
+    def summary(self, names=None):
+        if self.lib is None:
+            return {"error": self.error or "NVML unavailable"}
+        rows = [r for n, v in self.samples.items() if names is None or n in names for r in v]
+        if not rows:
+            return {"error": "no sample"}
+        reasons = sorted({name for _, m in rows for bit, name in self.REASON_BITS.items() if m & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_min_mhz": min(r[0] for r in rows),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(rows),
+                "window": "timed region (NVML, in process)"}
 
 
 def source_digest(files) -> str:
@@ -232,19 +280,33 @@ def aggregate_tokens_per_s(world: int, batch: int, step_ms_max: float) -> float:
 
 
 # --------------------------------------------------------------------------
-# CPU baseline: the oracle, in a fresh single-threaded process
+# CPU baseline: the oracle, in fresh single-threaded processes
 # --------------------------------------------------------------------------
+def baseline_units(w):
+    """(sequence, KV head) units the CPU sample covers: the whole first
+    sequence of the small workload, one unit of the others."""
+    if w.context * w.n_kv_heads <= 16384:
+        return [(0, h) for h in range(w.n_kv_heads)]
+    return [(0, 0)]
+
+
 def cpu_worker(spec: str):
-    """Run the oracle's decode step on a bounded sample; print JSON."""
-    import numpy as np  # noqa: F401  (threads pinned by the parent's environment)
+    """Run the oracle's decode step on a bounded sample; print JSON.
+
+    The sample is a list of (sequence, KV head) units of the workload; only
+    their keys and values are generated (the same bytes as in the full
+    workload).  Their summaries are built once, outside the timed steps; a
+    timed step is select + attend for every listed unit."""
     import oracle as O
     import workloads as W
     d = json.loads(spec)
     w = W.get(d["config"])
-    seqs = d["seqs"]
-    w_s = w.with_(batch=seqs, seed=w.seed)      # the first `seqs` sequences' shapes and recipe
-    x = W.generate(w_s)
-    units = [(b, h) for b in range(seqs) for h in range(w.n_kv_heads)]
+    units = [tuple(u) for u in d["units"]]
+    seqs = 1 + max(b for b, _ in units)
+    w_s = w.with_(batch=seqs)                  # the first sequences' shapes and recipe
+    t0 = time.time()
+    x = W.generate(w_s, units=units)
+    t_gen = time.time() - t0
     summaries = {}
     t0 = time.time()
     for b, h in units:
@@ -260,20 +322,37 @@ def cpu_worker(spec: str):
         if rep >= d["warmup"]:
             times.append(dt)
     per_step = statistics.median(times)
-    print(json.dumps({"tokens_per_s": seqs / per_step, "step_s": per_step, "build_s": t_build,
-                      "units": len(units), "seqs": seqs, "steps": len(times)}))
+    tokens = len(units) / w.n_kv_heads         # a token of one sequence needs every KV head
+    print(json.dumps({"tokens_per_s": tokens / per_step, "step_s": per_step, "steps_s": times,
+                      "build_s": t_build, "gen_s": t_gen, "units": len(units),
+                      "tokens_per_step": tokens, "steps": len(times)}))
 
 
-def run_cpu_baseline(config: str, seqs: int, steps: int, warmup: int):
+def start_cpu_baseline(config: str, units, steps: int, warmup: int):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
-    spec = json.dumps({"config": config, "seqs": seqs, "steps": steps, "warmup": warmup})
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", spec],
-                       capture_output=True, text=True, env=env, timeout=1800)
-    if r.returncode != 0:
-        raise RuntimeError("oracle worker failed: " + r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    spec = json.dumps({"config": config, "units": [list(u) for u in units], "steps": steps,
+                       "warmup": warmup})
+    return subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-worker", spec],
+                            stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env)
+
+
+def finish_cpu_baseline(proc, timeout=1800):
+    out, err = proc.communicate(timeout=timeout)
+    if proc.returncode != 0:
+        raise RuntimeError("oracle worker failed: " + err[-2000:])
+    return json.loads(out.strip().splitlines()[-1])
+
+
+def cpu_baseline_entry(w, res):
+    return {"value": res["tokens_per_s"], "unit": "tokens/s", "cores": 1,
+            "host_cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{res['units']} of {w.batch * w.n_kv_heads} (sequence, KV head) units of "
+                      f"{w.name} per step ({res['tokens_per_step']:g} token of one sequence's "
+                      f"layer step); fp64 NumPy oracle, one thread, median of {res['steps']} "
+                      f"steps of select + attend (summaries built once outside, "
+                      f"{res['build_s']:.1f} s)"}
 
 
 # --------------------------------------------------------------------------
@@ -284,24 +363,22 @@ def run_reference(args):
     if rank != 0:
         return 0
     import workloads as W
-    w = W.get(args.config)
-    seqs = 1
+    _, head = config_list(args.config)
+    w = W.get(head)
+    units = baseline_units(w)
     t0 = time.time()
-    res = run_cpu_baseline(args.config, seqs, max(1, args.steps), max(0, args.warmup))
+    res = finish_cpu_baseline(start_cpu_baseline(head, units, max(1, args.steps),
+                                                 max(0, args.warmup)))
     wall = time.time() - t0
     value = res["tokens_per_s"]
-    sample = (f"{seqs} of {w.batch} sequences ({res['units']} (sequence, KV head) units) of "
-              f"{args.config}; oracle summaries built once ({res['build_s']:.1f} s) outside the "
-              f"timed step; median of {res['steps']} steps")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": res["step_s"] * 1e3 * w.batch / seqs,
+        "ms_per_step": statistics.mean(res["steps_s"]) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "batch": w.batch,
                                         "context": w.context, "description": w.description},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": cpu_baseline_entry(w, res),
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "wall_s": wall,
@@ -339,38 +416,68 @@ def algorithmic_bytes(layer, inputs, selected):
     return select_bytes, decode_bytes, dense_bytes
 
 
-def run_gpu(args):
+class Timer:
+    """Event-timed loops on one stream with an L2 flush before every
+    iteration: write 256 MiB (> the 129 MB L2), then read another 256 MiB so
+    the dirty lines are written back before the timed work."""
+
+    def __init__(self, torch, stream, dist):
+        self.torch, self.stream, self.dist = torch, stream, dist
+        self.flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+        self.flush_rd = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+        self.flush_sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def flush_l2(self, i):
+        self.flush.fill_(float(i & 7))
+        self.torch.sum(self.flush_rd, dim=0, out=self.flush_sink)
+
+    def run(self, fn, n_steps, n_warm, region=None):
+        """fn(ev) with ev = (start, end) events to record around the timed
+        work, or None during warm-up; returns per-iteration milliseconds."""
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_steps)]
+        for i in range(n_warm):
+            self.flush_l2(i)
+            fn(None)
+        torch.cuda.synchronize()
+        if self.dist:
+            self.dist.barrier()
+        torch.cuda.synchronize()
+        ctx = region if region is not None else _Null()
+        with ctx:
+            for i in range(n_steps):
+                self.flush_l2(i)
+                fn(evs[i])
+            torch.cuda.synchronize()
+        if self.dist:
+            self.dist.barrier()
+        return [a.elapsed_time(b) for a, b in evs]
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def stats_us(ms):
+    s = sorted(ms)
+    n = len(s)
+    return {"mean": sum(s) / n * 1e3, "median": statistics.median(s) * 1e3,
+            "p10": s[n // 10] * 1e3, "p90": s[(9 * n) // 10] * 1e3}
+
+
+def measure_record(layer, inputs, timer, K, Wm, sampler, tag, full, args, world, dist):
+    """Build, then time the sparse step and its parts on one layer."""
     import numpy as np
     import torch
-    import workloads as W
-    from sparse_paged_kv_gb300 import binding as Bd
-    from sparse_paged_kv_gb300 import build_lib, runtime
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    # the oracle baseline runs first, in a fresh process, before this one does heavy GPU work
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_steps = 3
-        cpu = run_cpu_baseline(args.config, 1, cpu_steps, 1)
-
-    build_lib.build()
-    Bd.load_library()
-    w = replica_workload(W.get(args.config), rank)
-    t0 = time.time()
-    inputs = W.generate(w)
-    gen_s = time.time() - t0
-    sdt = {"f32": Bd.LOCKS_SUMMARY_F32, "bf16": Bd.LOCKS_SUMMARY_BF16,
-           "i4": Bd.LOCKS_SUMMARY_I4}[args.summary]
-    layer = runtime.LocksLayer.from_inputs(inputs, summary_dtype=sdt)
+    from sparse_paged_kv_gb300 import runtime
+    w = inputs.workload
     stream = torch.cuda.current_stream()
+    res = {}
 
     # ---- summary build (one-time, reported separately) ----
     ids = runtime.complete_page_blocks(inputs.block_table, inputs.seq_lens, w.page_size)
@@ -378,7 +485,6 @@ def run_gpu(args):
     bstat = torch.zeros((len(ids), w.n_kv_heads), dtype=torch.int32, device="cuda")
     tail = torch.zeros((len(ids), w.n_kv_heads), dtype=torch.float32, device="cuda")
     layer.build(ids_t, status=bstat, tail_energy=tail)
-    captured = captured_energy(layer, ids_t, tail, w)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     build_ms = []
@@ -391,57 +497,41 @@ def run_gpu(args):
     build_ms = min(build_ms)
     page_heads = len(ids) * w.n_kv_heads
     bstat_np = bstat.cpu().numpy()
-    not_conv = int(((bstat_np >> 16) != 0).sum())
     build_flops = build_flop_count(bstat_np & 0xFFFF, w.page_size, r=w.rank)
-
-    # In a decode loop each sequence completes a page every B steps and its
-    # summary is built then (off the step's critical path, section 4): time the
-    # build of one page per sequence (its last complete page, every KV head).
-    last = torch.from_numpy(np.array(
-        [inputs.block_table[b, max(0, int(inputs.seq_lens[b]) // w.page_size - 1)]
-         for b in range(w.batch)], dtype=np.int32)).cuda()
-    for _ in range(3):
-        layer.build(last)
-    torch.cuda.synchronize()
-    crossing_us = []
-    for _ in range(20):
-        e0.record(stream)
-        layer.build(last)
-        e1.record(stream)
+    res["build"] = {"ms": build_ms, "page_heads": page_heads,
+                    "pages_per_s": len(ids) / (build_ms / 1e3),
+                    "page_heads_per_s": page_heads / (build_ms / 1e3),
+                    "not_converged": int(((bstat_np >> 16) != 0).sum()),
+                    "mean_sweeps": float((bstat_np & 0xFFFF).mean()) if bstat_np.size else 0.0,
+                    "roofline": {"bound": "alu",
+                                 "achieved": build_flops / (build_ms / 1e3) / 1e12,
+                                 "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                                 "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+                                 "frac": build_flops / (build_ms / 1e3) / 1e12 / FP32_ALU_TFLOPS,
+                                 "flops": build_flops}}
+    if full:
+        res["build"]["captured_energy"] = captured_energy(layer, ids_t, tail, w)
+        # In a decode loop each sequence completes a page every B decode steps
+        # and its summary is built then (off the step's critical path, section
+        # 4): time the build of one page per sequence (its last complete page,
+        # every KV head).
+        last = torch.from_numpy(np.array(
+            [inputs.block_table[b, max(0, int(inputs.seq_lens[b]) // w.page_size - 1)]
+             for b in range(w.batch)], dtype=np.int32)).cuda()
+        for _ in range(3):
+            layer.build(last)
         torch.cuda.synchronize()
-        crossing_us.append(e0.elapsed_time(e1) * 1e3)
-    crossing_us = statistics.median(crossing_us)
-
-    # L2 flush between steps: write 256 MiB (> the 129 MB L2), then read another
-    # 256 MiB so the dirty lines are written back before the next timed step
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
-    flush_rd = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
-    flush_sink = torch.empty((), dtype=torch.float32, device="cuda")
-
-    def flush_l2(i):
-        flush.fill_(float(i & 7))
-        torch.sum(flush_rd, dim=0, out=flush_sink)
-
-    K, Wm = args.steps, args.warmup
-
-    def timed(fn, n_steps, n_warm, marks=3):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(n_steps)]
-        for i in range(n_warm):
-            flush_l2(i)
-            fn(None)
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter()
-        for i in range(n_steps):
-            flush_l2(i)
-            fn(evs[i])
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        t_wall = time.perf_counter() - t_wall
-        return evs, t_wall
+        cr = []
+        for _ in range(20):
+            e0.record(stream)
+            layer.build(last)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            cr.append(e0.elapsed_time(e1) * 1e3)
+        cr = statistics.median(cr)
+        res["build"].update({"page_crossing_us": cr, "page_crossing_per_step_us": cr / w.page_size,
+                             "page_crossing_note": "one completed page per sequence (all KV heads) "
+                                                   "built every B decode steps; amortised per step"})
 
     # ---- sparse step: select + sparse decode (events only at step bounds, so
     # the decode's programmatic launch overlaps the selection's tail) ----
@@ -453,43 +543,37 @@ def run_gpu(args):
         if ev:
             ev[1].record(stream)
 
-    sampler = ClockSampler(local)
-    sampler.start()
     for i in range(max(Wm, 3)):          # clock ramp
-        flush_l2(i)
+        timer.flush_l2(i)
         step(None)
     torch.cuda.synchronize()
-    sampler.mark_begin()
-    evs, wall = timed(step, K, Wm, marks=2)
-    sampler.mark_end()
-    clocks = sampler.stop()
-    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    status = int(layer.status.cpu()[0])
+    t_wall = time.perf_counter()
+    step_ms = timer.run(step, K, Wm, sampler.region(f"{tag}:step"))
+    res["wall_timed_s"] = time.perf_counter() - t_wall
+    res["step_ms"] = step_ms
+    res["status"] = int(layer.status.cpu()[0])
     selected = layer.selected.cpu().numpy()
-    select_bytes, decode_bytes, dense_bytes = algorithmic_bytes(layer, inputs, selected)
-    mean_step = sum(step_ms) / K
-    mean_step_max = reduce_max(mean_step, dist, "cuda")
+    res["bytes"] = algorithmic_bytes(layer, inputs, selected)
+    res["step_mean_max_ms"] = reduce_max(sum(step_ms) / K, dist, "cuda")
 
     # ---- the same step replayed from a CUDA graph ----
-    graph_ms, graph_err = None, None
-    try:
-        graph = layer.capture_step()
+    res["graph_ms"], res["graph_error"] = None, None
+    if full:
+        try:
+            graph = layer.capture_step()
 
-        def gstep(ev):
-            if ev:
-                ev[0].record(stream)
-            graph.replay()
-            if ev:
-                ev[1].record(stream)
+            def gstep(ev):
+                if ev:
+                    ev[0].record(stream)
+                graph.replay()
+                if ev:
+                    ev[1].record(stream)
 
-        gevs, _ = timed(gstep, max(1, min(K, 500)), min(Wm, 10), marks=2)
-        graph_ms = [e[0].elapsed_time(e[1]) for e in gevs]
-    except RuntimeError as exc:          # reported in the JSON line, never hidden
-        graph_err = str(exc).splitlines()[0][:200]
+            res["graph_ms"] = timer.run(gstep, K, Wm)
+        except RuntimeError as exc:          # reported in the JSON line, never hidden
+            res["graph_error"] = str(exc).splitlines()[0][:200]
 
-    # ---- the two calls on their own (events between them), for the roofline ----
-    K2 = max(1, min(K, 200))
-
+    # ---- the two calls on their own, for the roofline ----
     def sel_only(ev):
         if ev:
             ev[0].record(stream)
@@ -497,8 +581,7 @@ def run_gpu(args):
         if ev:
             ev[1].record(stream)
 
-    sevs, _ = timed(sel_only, K2, min(Wm, 10), marks=2)
-    sel_ms = [e[0].elapsed_time(e[1]) for e in sevs]
+    res["sel_ms"] = timer.run(sel_only, K, Wm, sampler.region(f"{tag}:select"))
 
     def dec_only(ev):
         layer.select()
@@ -508,28 +591,11 @@ def run_gpu(args):
         if ev:
             ev[1].record(stream)
 
-    devs_, _ = timed(dec_only, K2, min(Wm, 10), marks=2)
-    dec_ms = [e[0].elapsed_time(e[1]) for e in devs_]
-
-    # ---- dense comparison ----
-    dense = None
-    if not args.no_dense:
-        def dstep(ev):
-            if ev:
-                ev[0].record(stream)
-            layer.dense_decode()
-            if ev:
-                ev[1].record(stream)
-        devs, _ = timed(dstep, K, Wm, marks=2)
-        dms = [e[0].elapsed_time(e[1]) for e in devs]
-        dmean = sum(dms) / K
-        dense = {"tokens_per_s": w.batch / (dmean / 1e3), "us_per_step": dmean * 1e3,
-                 "us_median": statistics.median(dms) * 1e3,
-                 "gbs": dense_bytes / (dmean / 1e3) / 1e9, "bytes_per_step": dense_bytes}
+    res["dec_ms"] = timer.run(dec_only, K, Wm)
 
     # ---- end to end through the public API, host buffers ----
-    e2e = None
-    if not args.no_e2e:
+    res["e2e"] = None
+    if full and not args.no_e2e:
         q_host = layer.q.cpu().pin_memory()
         out_host = torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory()
 
@@ -541,12 +607,125 @@ def run_gpu(args):
             out_host.copy_(layer.out, non_blocking=True)
             if ev:
                 ev[1].record(stream)
-        eevs, _ = timed(estep, K, Wm, marks=2)
-        ems = reduce_max(sum(e[0].elapsed_time(e[1]) for e in eevs) / K, dist, "cuda")
-        e2e = {"value": aggregate_tokens_per_s(world, w.batch, ems), "unit": "tokens/s",
-               "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
-               "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
-               "us_per_step": ems * 1e3}
+        ems = reduce_max(sum(timer.run(estep, K, Wm)) / K, dist, "cuda")
+        res["e2e"] = {"value": aggregate_tokens_per_s(world, w.batch, ems), "unit": "tokens/s",
+                      "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+                      "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
+                      "us_per_step": ems * 1e3}
+    return res
+
+
+def measure_dense(layer, inputs, timer, K, Wm, sampler, tag):
+    import torch
+    stream = torch.cuda.current_stream()
+
+    def dstep(ev):
+        if ev:
+            ev[0].record(stream)
+        layer.dense_decode()
+        if ev:
+            ev[1].record(stream)
+    return timer.run(dstep, K, Wm, sampler.region(f"{tag}:dense"))
+
+
+def summarise(w, res, peak, world, dense_ms=None):
+    """Per-workload numbers of one record type."""
+    select_bytes, decode_bytes, dense_bytes = res["bytes"]
+    step = stats_us(res["step_ms"])
+    sel_us = stats_us(res["sel_ms"])["mean"]
+    dec_us = stats_us(res["dec_ms"])["mean"]
+    step_gbs = (select_bytes + decode_bytes) / (step["mean"] / 1e6) / 1e9
+    sel_gbs = select_bytes / (sel_us / 1e6) / 1e9
+    out = {"step_us": step, "tokens_per_s": aggregate_tokens_per_s(world, w.batch,
+                                                                     res["step_mean_max_ms"]),
+           "select_alone_us": sel_us, "sparse_decode_alone_us": dec_us,
+           "select_gbs": sel_gbs, "select_frac": sel_gbs / peak,
+           "sparse_decode_gbs": decode_bytes / (dec_us / 1e6) / 1e9,
+           "sparse_decode_frac": decode_bytes / (dec_us / 1e6) / 1e9 / peak,
+           "step_gbs": step_gbs, "step_frac": step_gbs / peak,
+           "select_bytes": select_bytes, "sparse_decode_bytes": decode_bytes,
+           "build_page_heads_per_s": res["build"]["page_heads_per_s"],
+           "device_status": res["status"]}
+    if res.get("graph_ms"):
+        out["graph_replay_us"] = stats_us(res["graph_ms"])
+    if res.get("graph_error"):
+        out["graph_error"] = res["graph_error"]
+    if dense_ms is not None:
+        d = stats_us(dense_ms)
+        out["dense"] = {"us": d["mean"], "us_median": d["median"],
+                        "tokens_per_s": w.batch / (d["mean"] / 1e6),
+                        "gbs": dense_bytes / (d["mean"] / 1e6) / 1e9,
+                        "frac": dense_bytes / (d["mean"] / 1e6) / 1e9 / peak,
+                        "bytes_per_step": dense_bytes}
+        out["speedup_vs_dense"] = d["mean"] / step["mean"]
+    return out
+
+
+def run_gpu(args):
+    import torch
+    import workloads as W
+    from sparse_paged_kv_gb300 import binding as Bd
+    from sparse_paged_kv_gb300 import build_lib, runtime
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    names, head = config_list(args.config)
+    extras = [s for s in args.extra_summary.split(",") if s and s != args.summary]
+    SDT = {"f32": Bd.LOCKS_SUMMARY_F32, "bf16": Bd.LOCKS_SUMMARY_BF16, "i4": Bd.LOCKS_SUMMARY_I4}
+
+    # the oracle baselines run first, in fresh single-threaded processes (one
+    # per workload, side by side), before this one does any GPU work
+    cpu = {}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        procs = {n: start_cpu_baseline(n, baseline_units(W.get(n)), 3, 1) for n in names}
+        for n, p in procs.items():
+            cpu[n] = finish_cpu_baseline(p)
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build_lib.build()
+    Bd.load_library()
+    sampler = ClockSampler(local)
+    timer = Timer(torch, torch.cuda.current_stream(), dist)
+    peak, peak_kind = measured_peaks()
+    K, Wm = args.steps, args.warmup
+
+    per_config, headline = {}, None
+    for name in names:
+        w = replica_workload(W.get(name), rank)
+        t0 = time.time()
+        inputs = W.generate(w)
+        gen_s = time.time() - t0
+        layer = runtime.LocksLayer.from_inputs(inputs, summary_dtype=SDT[args.summary])
+        is_head = name == head
+        res = measure_record(layer, inputs, timer, K, Wm, sampler, f"{name}:{args.summary}",
+                             is_head, args, world, dist)
+        dense_ms = None if args.no_dense else measure_dense(layer, inputs, timer, K, Wm, sampler,
+                                                            name)
+        entry = {"workload": name, "batch": w.batch, "context": w.context,
+                 "k_pages": layer.k, "input_gen_s": gen_s}
+        entry[args.summary] = summarise(w, res, peak, world, dense_ms)
+        for ex in extras:
+            other = layer.sharing_inputs(SDT[ex])
+            r2 = measure_record(other, inputs, timer, K, Wm, sampler, f"{name}:{ex}", False,
+                                args, world, dist)
+            s2 = summarise(w, r2, peak, world, None)
+            if dense_ms is not None:
+                s2["speedup_vs_dense"] = stats_us(dense_ms)["mean"] / s2["step_us"]["mean"]
+            entry[ex] = s2
+            del other
+        if name in cpu:
+            entry["cpu_baseline"] = cpu_baseline_entry(w, cpu[name])
+        per_config[name] = entry
+        if is_head:
+            headline = (w, res, entry)
+        del layer, inputs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
 
     if dist:
         dist.barrier()
@@ -555,18 +734,17 @@ def run_gpu(args):
             dist.destroy_process_group()
         return 0
 
-    peak, peak_kind = measured_peaks()
-    sel_mean = sum(sel_ms) / len(sel_ms)
-    achieved = select_bytes / (sel_mean / 1e3) / 1e9
-    traffic, prof = profile_traffic("select", w.name if args.summary == "f32"
-                                    else f"{w.name}_{args.summary}")
-    step_gbs = (select_bytes + decode_bytes) / (mean_step / 1e3) / 1e9
+    w, res, entry = headline
+    main = entry[args.summary]
+    select_bytes, decode_bytes, _ = res["bytes"]
+    traffic, _ = profile_traffic("select", w.name if args.summary == "f32"
+                                 else f"{w.name}_{args.summary}")
     line = {
         "metric": METRIC,
-        "value": aggregate_tokens_per_s(world, w.batch, mean_step_max),
+        "value": main["tokens_per_s"],
         "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": Wm,
-        "ms_per_step": mean_step_max,
+        "ms_per_step": res["step_mean_max_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
@@ -576,49 +754,31 @@ def run_gpu(args):
                    "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read)",
                    "step": "locks_select + locks_sparse_decode, one layer",
                    "parallelism": f"replicas x{world}"},
-        "step_us": {"mean": mean_step * 1e3, "median": statistics.median(step_ms) * 1e3,
-                    "p10": sorted(step_ms)[K // 10] * 1e3, "p90": sorted(step_ms)[(9 * K) // 10] * 1e3,
-                    "select_alone_mean": sel_mean * 1e3,
-                    "sparse_decode_alone_mean": sum(dec_ms) / len(dec_ms) * 1e3,
-                    "graph_replay_mean": (sum(graph_ms) / len(graph_ms) * 1e3) if graph_ms else None,
-                    "graph_replay_median": statistics.median(graph_ms) * 1e3 if graph_ms else None},
-        "graph_error": graph_err,
-        "step_gbs": step_gbs,
-        "step_frac": step_gbs / peak,
+        "step_us": main["step_us"],
+        "select_alone_us": main["select_alone_us"],
+        "sparse_decode_alone_us": main["sparse_decode_alone_us"],
+        "graph_replay_us": main.get("graph_replay_us"),
+        "step_gbs": main["step_gbs"],
+        "step_frac": main["step_frac"],
         "roofline": {"bound": "hbm", "kernel": "locks_select (score_kernel + finalize_kernel)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": traffic,
+                     "achieved": main["select_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": main["select_frac"], "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes": select_bytes},
-        "sparse_decode": {"gbs": decode_bytes / (sum(dec_ms) / len(dec_ms) / 1e3) / 1e9,
+        "sparse_decode": {"gbs": main["sparse_decode_gbs"], "frac": main["sparse_decode_frac"],
                           "bytes_per_step": decode_bytes},
-        "dense": dense,
-        "speedup_vs_dense": (dense["us_per_step"] / (mean_step * 1e3)) if dense else None,
-        "build": {"ms": build_ms, "page_heads": page_heads, "pages_per_s": len(ids) / (build_ms / 1e3),
-                  "page_heads_per_s": page_heads / (build_ms / 1e3), "not_converged": not_conv,
-                  "mean_sweeps": float((bstat_np & 0xFFFF).mean()),
-                  "roofline": {"bound": "alu", "achieved": build_flops / (build_ms / 1e3) / 1e12,
-                               "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
-                               "frac": build_flops / (build_ms / 1e3) / 1e12 / FP32_ALU_TFLOPS,
-                               "flops": build_flops},
-                  "captured_energy": captured,
-                  "page_crossing_us": crossing_us,
-                  "page_crossing_per_step_us": crossing_us / w.page_size,
-                  "page_crossing_fraction_of_step": crossing_us / w.page_size / (mean_step * 1e3),
-                  "page_crossing_note": "one completed page per sequence (all KV heads) "
-                                        "built every B decode steps; amortised per step"},
-        "e2e": e2e,
-        "gpu_launches": 3 * K,
-        "clocks": clocks,
-        "device_status": status,
-        "input_gen_s": gen_s,
-        "wall_timed_s": wall,
+        "dense": main.get("dense"),
+        "speedup_vs_dense": main.get("speedup_vs_dense"),
+        "build": res["build"],
+        "e2e": res["e2e"],
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "clocks": sampler.summary([f"{w.name}:{args.summary}:step"]),
+        "clocks_all_regions": sampler.summary(),
+        "device_status": res["status"],
+        "wall_timed_s": res["wall_timed_s"],
+        "per_config": per_config,
     }
-    if cpu is not None:
-        line["cpu_baseline"] = {"value": cpu["tokens_per_s"], "unit": "tokens/s", "cores": 1,
-                                "kind": "oracle",
-                                "sample": f"1 of {w.batch} sequences ({cpu['units']} units) of "
-                                          f"{w.name}, median of {cpu['steps']} oracle steps "
-                                          f"(select + attend; summaries prebuilt)"}
+    if w.name in cpu:
+        line["cpu_baseline"] = entry["cpu_baseline"]
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()

@@ -7,6 +7,7 @@ library's kernels.
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 from typing import Optional
 
@@ -76,6 +77,16 @@ class LocksLayer:
         w = inputs.workload
         cfg = B.LocksConfig.from_workload(w, summary_dtype)
         return cls(cfg, w.budget_tokens if budget_tokens is None else budget_tokens).load_inputs(inputs)
+
+    def sharing_inputs(self, summary_dtype: int) -> "LocksLayer":
+        """A layer over the same device inputs (q, K/V pools, block table,
+        sequence lengths) with its own summary pool of another record type."""
+        cfg = dataclasses.replace(self.cfg, summary_dtype=int(summary_dtype))
+        other = LocksLayer(cfg, self.budget, self.device)
+        for name in ("q", "k_cache", "v_cache", "block_table", "seq_lens", "host_block_table",
+                     "host_seq_lens"):
+            setattr(other, name, getattr(self, name))
+        return other
 
     # ---- calls ----------------------------------------------------------------
     def build(self, block_ids=None, tail_energy=None, status=None, max_sweeps: int = 0):

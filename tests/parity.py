@@ -21,6 +21,7 @@ score and reconstruction gates; they are counted.
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass, field
 from typing import Dict, List, Tuple
 
@@ -32,6 +33,13 @@ LSE_TOL = 1e-3
 OUT_TOL = 2e-2
 OUT_LSE_TOL = 1e-3
 TIE_TOL = 1e-5
+# averaged shares m_bar, element by element: within the tie window in absolute
+# terms, and within the relative change that the s_hat gate allows -- every
+# s_hat within LSE_TOL moves log Z by at most LSE_TOL too, so each share
+# exp(s_hat - log Z) by at most a factor e^{2 LSE_TOL}, and so their mean;
+# 1e-5 more covers the float32 exponentials and sums
+SHARE_ABS_TOL = TIE_TOL
+SHARE_REL_TOL = math.expm1(2 * LSE_TOL) + 1e-5
 RECON_TOL = 1e-4
 RECON_GAP_COEF = 2e-5
 SIGMA_TOL = 1e-4
@@ -57,6 +65,11 @@ class Report:
     max_recon_rel: float = 0.0
     max_sigma_rel: float = 0.0
     max_record_err: float = 0.0
+    max_share_abs: float = 0.0
+    max_share_rel: float = 0.0
+    # largest e_rec * gap over the gated pages: the coefficient the
+    # reconstruction gate max(RECON_TOL, RECON_GAP_COEF / gap) actually needed
+    max_recon_gap: float = 0.0
     failures: List[str] = field(default_factory=list)
 
     def fail(self, msg):
@@ -130,6 +143,7 @@ def compare_build(layer, inputs, res: O.UnitResult, rep: Report, tail=None, stat
         e_rec = np.abs(rec_gpu - rec_ref).max() / scale
         rep.max_recon_rel = max(rep.max_recon_rel, e_rec)
         gap = (s.sigma2[r - 1] - s.sigma2[r]) / s.sigma2[0] if len(s.sigma2) > r else 1.0
+        rep.max_recon_gap = max(rep.max_recon_gap, e_rec * gap)
         tol = max(RECON_TOL, RECON_GAP_COEF / gap)
         if e_rec > tol:
             rep.fail(f"reconstruction b{b} h{h} p{j}: {e_rec:.2e} (relative gap {gap:.2e})")
@@ -160,6 +174,13 @@ def compare_select(layer, snap, res: O.UnitResult, rep: Report):
         sh = snap["page_share"][b, h][sel.cand]
         if abs(sh.sum() - 1.0) > 1e-4:
             rep.fail(f"shares b{b} h{h} sum to {sh.sum()}")
+        if not degen:                     # a degenerate page's s_hat is not gated
+            err = np.abs(sh - sel.mbar)
+            rel = float((err / np.maximum(sel.mbar, 1e-30)).max())
+            rep.max_share_abs = max(rep.max_share_abs, float(err.max()))
+            rep.max_share_rel = max(rep.max_share_rel, rel)
+            if not np.isfinite(err.max()) or err.max() > SHARE_ABS_TOL or rel > SHARE_REL_TOL:
+                rep.fail(f"shares b{b} h{h}: max abs err {err.max():.3e}, rel {rel:.3e}")
     got = [int(x) for x in snap["selected"][b, h] if x >= 0]
     want = [int(x) for x in sel.selected]
     if got != sorted(got) or len(set(got)) != len(got):

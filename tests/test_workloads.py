@@ -63,3 +63,17 @@ def test_bf16_rounding_is_nearest_even():
     assert back[1] == 1.0                        # tie -> even
     assert back[2] == 1.0 + 4 * 2 ** -8          # tie -> even (up)
     assert back[3] == -2.5
+
+
+def test_unit_subset_matches_full_workload():
+    """Generating only some (sequence, KV head) units gives those units the
+    bytes they have in the full workload and leaves every other page NaN."""
+    w = W.get("tiny")
+    full = W.generate(w)
+    part = W.generate(w, units=[(0, 1)])
+    blk = full.block_table[0, :w.max_pages]
+    assert np.array_equal(full.k_cache[blk, 1], part.k_cache[blk, 1])
+    assert np.array_equal(full.v_cache[blk, 1], part.v_cache[blk, 1])
+    assert np.array_equal(full.q, part.q)
+    assert np.array_equal(full.carriers[0][1], part.carriers[0][1])
+    assert (part.k_cache[blk, 0] == 0x7FC0).all() and (part.v_cache[blk, 0] == 0x7FC0).all()

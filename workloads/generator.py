@@ -31,7 +31,7 @@ import math
 import os
 from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
-from typing import List, Optional
+from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -137,8 +137,14 @@ def _gen_unit(w: LocksWorkload, b: int, h: int, seq_len: int, q_hat: np.ndarray,
     return carriers
 
 
-def generate(w: LocksWorkload, threads: Optional[int] = None) -> LocksInputs:
-    """Generate the inputs of workload ``w`` (deterministic in ``w.seed``)."""
+def generate(w: LocksWorkload, threads: Optional[int] = None,
+             units: Optional[Sequence[Tuple[int, int]]] = None) -> LocksInputs:
+    """Generate the inputs of workload ``w`` (deterministic in ``w.seed``).
+
+    ``units`` limits the keys and values filled to the listed (sequence, KV
+    head) pairs; every other page of the pools stays NaN.  Each unit draws
+    from its own streams, so a listed unit gets exactly the bytes it has in
+    the full workload."""
     assert w.n_q_heads % w.n_kv_heads == 0
     lens = w.lengths()
     B, d, Hk, Hq = w.page_size, w.head_dim, w.n_kv_heads, w.n_q_heads
@@ -160,11 +166,14 @@ def generate(w: LocksWorkload, threads: Optional[int] = None) -> LocksInputs:
     v_cache = np.full((w.num_blocks, Hk, B, d), BF16_NAN, dtype=np.uint16)
 
     jobs = []
+    want = None if units is None else {(int(b), int(h)) for b, h in units}
     for b, t in enumerate(lens):
         if t <= 0:
             continue
         n = math.ceil(t / B)
         for h in range(Hk):
+            if want is not None and (b, h) not in want:
+                continue
             s = q32[b, h * G:(h + 1) * G].sum(axis=0)
             q_hat = s / max(np.linalg.norm(s), 1e-30)
             jobs.append((b, h, t, q_hat, block_table[b, :n].astype(np.int64)))
