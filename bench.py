@@ -61,6 +61,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-loop", action="store_true", help="skip the decode-loop measurement")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -615,6 +616,63 @@ def measure_record(layer, inputs, timer, K, Wm, sampler, tag, full, args, world,
     return res
 
 
+def measure_decode_loop(layer, w, sampler, tag, reps=3):
+    """B consecutive decode-loop steps (locks_append_kv, locks_build_completed
+    on a side stream, select, sparse decode) starting from length T - B, so
+    the last step completes one page per sequence and its build runs as it
+    would in an engine; against B consecutive plain steps (select + sparse
+    decode) on the same inputs.  No L2 flush inside either run.  The
+    difference per step is the amortised cost of appending and of the
+    page-crossing refresh.  The appended rows overwrite the last page's keys
+    and values with new random ones; lengths end where they started."""
+    import torch
+    from sparse_paged_kv_gb300 import runtime
+    B = w.page_size
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device="cuda").manual_seed(99)
+    rows = torch.randn((B, 2, w.batch, w.n_kv_heads, w.head_dim), generator=g, device="cuda")
+    rows = rows.to(torch.bfloat16)
+    lens0 = layer.seq_lens.clone()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def plain():
+        e0.record(stream)
+        for _ in range(B):
+            layer.select()
+            layer.sparse_decode()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def looped():
+        layer.seq_lens.copy_(lens0 - B)
+        loop = runtime.DecodeLoop(layer)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for s in range(B):
+            loop.step(rows[s, 0], rows[s, 1])
+        loop.finish()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), loop
+
+    plain()
+    looped()
+    with sampler.region(f"{tag}:loop"):
+        p_ms = [plain() for _ in range(reps)]
+        l_out = [looped() for _ in range(reps)]
+    l_ms = [x[0] for x in l_out]
+    done = l_out[-1][1].completed[(B - 1) & 1].cpu().numpy()
+    ok = bool((done >= 0).all()) and torch.equal(layer.seq_lens, lens0)
+    p_us = statistics.median(p_ms) * 1e3 / B
+    l_us = statistics.median(l_ms) * 1e3 / B
+    return {"steps": B, "runs": reps, "plain_us_per_step": p_us, "loop_us_per_step": l_us,
+            "refresh_us_per_step": l_us - p_us, "refresh_fraction_of_step": (l_us - p_us) / p_us,
+            "pages_completed_per_run": int((done >= 0).sum()), "completions_as_expected": ok,
+            "note": "B consecutive steps, no L2 flush: append + build of the completed pages "
+                    "on a side stream + select + sparse decode, against select + sparse decode"}
+
+
 def measure_dense(layer, inputs, timer, K, Wm, sampler, tag):
     import torch
     stream = torch.cuda.current_stream()
@@ -718,6 +776,8 @@ def run_gpu(args):
                 s2["speedup_vs_dense"] = stats_us(dense_ms)["mean"] / s2["step_us"]["mean"]
             entry[ex] = s2
             del other
+        if not args.no_loop:
+            entry[args.summary]["decode_loop"] = measure_decode_loop(layer, w, sampler, name)
         if name in cpu:
             entry["cpu_baseline"] = cpu_baseline_entry(w, cpu[name])
         per_config[name] = entry
@@ -769,6 +829,7 @@ def run_gpu(args):
         "dense": main.get("dense"),
         "speedup_vs_dense": main.get("speedup_vs_dense"),
         "build": res["build"],
+        "decode_loop": main.get("decode_loop"),
         "e2e": res["e2e"],
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": sampler.summary([f"{w.name}:{args.summary}:step"]),

@@ -166,6 +166,47 @@ int locks_build_summaries(const locks_cfg_t* cfg, const void* k_cache, const int
                           int32_t max_sweeps, void* stream);
 
 /*
+ * locks_append_kv -- the cache write of one decode step, and the page
+ * completions it causes (section 4 "Build": a page is summarised once, when it
+ * completes; App. E (ii): one incremental build per finalised page).
+ *
+ * For every sequence b with t = seq_lens[b] on entry: the token's key and
+ * value rows of every KV head go to slot t % B of physical block
+ * block_table[b * max_pages + t / B]; seq_lens[b] becomes t + 1; and
+ * completed[b] is that block when t + 1 is a multiple of B (the token
+ * completed its page), else -1.  Allocating a block for a sequence's next
+ * page (writing the block-table entry before the step that starts the page)
+ * stays with the caller.  A sequence already holding max_pages * B tokens
+ * (LOCKS_DEV_BAD_SEQ_LEN) or whose entry is not a valid block
+ * (LOCKS_DEV_BAD_BLOCK_ID) is left unchanged, with completed[b] = -1.
+ *
+ *   k_new, v_new  bf16 [batch][n_kv_heads][d], 16-byte aligned
+ *   k_cache, v_cache  the pools, 16-byte aligned; written
+ *   seq_lens      int32 [batch]: read, then advanced
+ *   completed     nullable int32 [batch]: written
+ *   status        nullable int32[1]
+ * Pass `completed` to locks_build_completed (for example on a second stream
+ * that waits for this call): the page completed at step s is first a
+ * selection candidate at step s + 1, so its build may overlap step s's
+ * selection and decode and must finish before step s + 1's locks_select.
+ */
+int locks_append_kv(const locks_cfg_t* cfg, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* block_table, int32_t* seq_lens,
+                    int32_t* completed, int32_t* status, void* stream);
+
+/*
+ * locks_build_completed -- locks_build_summaries over a list in which an entry
+ * < 0 means "no page" and is skipped without a flag (its status entries are
+ * set to 0): the `completed` list that locks_append_kv writes, used as it
+ * stands on the device, so no host round trip decides which pages to build.
+ * Arguments as for locks_build_summaries, with block_ids = completed and
+ * n_blocks = n (the batch).
+ */
+int locks_build_completed(const locks_cfg_t* cfg, const void* k_cache, const int32_t* completed,
+                          int32_t n, void* summaries, float* tail_energy, int32_t* status,
+                          int32_t max_sweeps, void* stream);
+
+/*
  * locks_select -- section 4 "Score" (Eq. (1)), the page-mass share, the
  * share-average, and the forced-page top-(k-2) rule (section 2; Cor. 3).
  *

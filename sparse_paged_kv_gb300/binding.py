@@ -105,6 +105,10 @@ _SIGS = {
                                           _P, ctypes.c_size_t, _P, _P]),
     "locks_select_noalloc": (ctypes.c_int, [ctypes.POINTER(locks_cfg_t), _P, _P, _P, _P,
                                             ctypes.c_int32, _P, _P, _P, _P, _P]),
+    "locks_append_kv": (ctypes.c_int, [ctypes.POINTER(locks_cfg_t), _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P]),
+    "locks_build_completed": (ctypes.c_int, [ctypes.POINTER(locks_cfg_t), _P, _P, ctypes.c_int32,
+                                             _P, _P, _P, ctypes.c_int32, _P]),
     "locks_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "locks_abi_version": (ctypes.c_int, []),
 }
@@ -183,6 +187,22 @@ def locks_build_summaries(cfg: LocksConfig, k_cache, block_ids, summaries, tail_
         ctypes.byref(cfg.c()), _ptr(k_cache), _ptr(block_ids), int(n_blocks), _ptr(summaries),
         _ptr(tail_energy), _ptr(status), int(max_sweeps), _stream(stream))
     _check("locks_build_summaries", rc)
+
+
+def locks_append_kv(cfg: LocksConfig, k_new, v_new, k_cache, v_cache, block_table, seq_lens,
+                    completed=None, status=None, stream=None) -> None:
+    rc = load_library().locks_append_kv(
+        ctypes.byref(cfg.c()), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_table), _ptr(seq_lens), _ptr(completed), _ptr(status), _stream(stream))
+    _check("locks_append_kv", rc)
+
+
+def locks_build_completed(cfg: LocksConfig, k_cache, completed, summaries, tail_energy=None,
+                          status=None, max_sweeps: int = 0, stream=None) -> None:
+    rc = load_library().locks_build_completed(
+        ctypes.byref(cfg.c()), _ptr(k_cache), _ptr(completed), int(completed.numel()),
+        _ptr(summaries), _ptr(tail_energy), _ptr(status), int(max_sweeps), _stream(stream))
+    _check("locks_build_completed", rc)
 
 
 def locks_select(cfg: LocksConfig, q, summaries, block_table, seq_lens, budget_tokens: int,

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libsparse_paged_kv.so")
 SOURCES = ["locks_api.cu", "locks_build.cu", "locks_select.cu", "locks_score_b16.cu",
-           "locks_decode.cu", "locks_select_noalloc.cu"]
+           "locks_decode.cu", "locks_select_noalloc.cu", "locks_append.cu"]
 HEADERS = ["locks_common.cuh", "locks_internal.h", "locks_score.cuh", "locks_topk.cuh",
            "locks_mma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

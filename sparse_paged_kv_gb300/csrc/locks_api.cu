@@ -141,6 +141,35 @@ int decode_common(const locks_cfg_t* cfg, const void* q, const void* k_cache, co
 
 }  // namespace
 
+namespace {
+
+int build_common(const locks_cfg_t* cfg, const void* k_cache, const int32_t* block_ids,
+                 int32_t n_blocks, void* summaries, float* tail_energy, int32_t* status,
+                 int32_t max_sweeps, int skip_negative, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc != LOCKS_OK) return rc;
+  if (n_blocks < 0 || max_sweeps < 0) return LOCKS_ERR_INVALID_ARG;
+  if (n_blocks == 0) return LOCKS_OK;
+  if (!k_cache || !block_ids || !summaries) return LOCKS_ERR_INVALID_ARG;
+  locks::BuildParams p;
+  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  p.block_ids = block_ids;
+  p.summaries = summaries;
+  p.tail_energy = tail_energy;
+  p.status = status;
+  p.rec_bytes = locks_summary_record_bytes(cfg);
+  p.n_blocks = n_blocks;
+  p.n_kv_heads = cfg->n_kv_heads;
+  p.num_blocks = cfg->num_blocks;
+  p.rank = cfg->rank;
+  p.max_sweeps = max_sweeps == 0 ? 20 : max_sweeps;
+  p.skip_negative = skip_negative;
+  return locks::launch_build(p, locks::rank_cap(cfg->rank), cfg->summary_dtype, cfg->page_size,
+                             static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t locks_summary_record_bytes(const locks_cfg_t* cfg) {
@@ -170,25 +199,42 @@ size_t locks_decode_workspace_bytes(const locks_cfg_t* cfg, int32_t n_pages) {
 int locks_build_summaries(const locks_cfg_t* cfg, const void* k_cache, const int32_t* block_ids,
                           int32_t n_blocks, void* summaries, float* tail_energy, int32_t* status,
                           int32_t max_sweeps, void* stream) {
+  return build_common(cfg, k_cache, block_ids, n_blocks, summaries, tail_energy, status,
+                      max_sweeps, 0, stream);
+}
+
+int locks_build_completed(const locks_cfg_t* cfg, const void* k_cache, const int32_t* completed,
+                          int32_t n, void* summaries, float* tail_energy, int32_t* status,
+                          int32_t max_sweeps, void* stream) {
+  return build_common(cfg, k_cache, completed, n, summaries, tail_energy, status, max_sweeps, 1,
+                      stream);
+}
+
+int locks_append_kv(const locks_cfg_t* cfg, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* block_table, int32_t* seq_lens,
+                    int32_t* completed, int32_t* status, void* stream) {
   int rc = check_cfg(cfg);
   if (rc != LOCKS_OK) return rc;
-  if (n_blocks < 0 || max_sweeps < 0) return LOCKS_ERR_INVALID_ARG;
-  if (n_blocks == 0) return LOCKS_OK;
-  if (!k_cache || !block_ids || !summaries) return LOCKS_ERR_INVALID_ARG;
-  locks::BuildParams p;
-  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-  p.block_ids = block_ids;
-  p.summaries = summaries;
-  p.tail_energy = tail_energy;
+  if (cfg->batch == 0) return LOCKS_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !seq_lens)
+    return LOCKS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+       reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return LOCKS_ERR_INVALID_ARG;                     // rows move as 16-byte words
+  locks::AppendParams p;
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.completed = completed;
   p.status = status;
-  p.rec_bytes = locks_summary_record_bytes(cfg);
-  p.n_blocks = n_blocks;
   p.n_kv_heads = cfg->n_kv_heads;
+  p.max_pages = cfg->max_pages;
   p.num_blocks = cfg->num_blocks;
-  p.rank = cfg->rank;
-  p.max_sweeps = max_sweeps == 0 ? 20 : max_sweeps;
-  return locks::launch_build(p, locks::rank_cap(cfg->rank), cfg->summary_dtype, cfg->page_size,
-                             static_cast<cudaStream_t>(stream));
+  p.page_size = cfg->page_size;
+  return locks::launch_append(p, cfg->batch, static_cast<cudaStream_t>(stream));
 }
 
 int locks_select(const locks_cfg_t* cfg, const void* q, const void* summaries,

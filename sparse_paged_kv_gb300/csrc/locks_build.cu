@@ -281,7 +281,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   const int out_idx = pid * prm.n_kv_heads + h;
   const int blk = prm.block_ids[pid];
   if (blk < 0 || blk >= prm.num_blocks) {
-    if (tid == 0 && prm.status) prm.status[out_idx] = LOCKS_DEV_BAD_BLOCK_ID << 16;
+    if (tid == 0 && prm.status)
+      prm.status[out_idx] = (prm.skip_negative && blk < 0) ? 0 : LOCKS_DEV_BAD_BLOCK_ID << 16;
     return;
   }
 

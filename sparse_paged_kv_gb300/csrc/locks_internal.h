@@ -79,6 +79,19 @@ struct BuildParams {
   int32_t* status;               // nullable [n_blocks][H_kv]
   size_t rec_bytes;
   int n_blocks, n_kv_heads, num_blocks, rank, max_sweeps;
+  int skip_negative;             // a negative block id means "no page": skipped, not flagged
+};
+
+struct AppendParams {
+  const __nv_bfloat16* k_new;    // [batch][H_kv][d]
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_cache;        // [num_blocks][H_kv][B][d]
+  __nv_bfloat16* v_cache;
+  const int32_t* block_table;    // [batch][max_pages]
+  int32_t* seq_lens;             // [batch], advanced by one
+  int32_t* completed;            // nullable [batch]
+  int32_t* status;               // nullable
+  int n_kv_heads, max_pages, num_blocks, page_size;
 };
 
 // ctas_per_sm: score CTAs per SM the grid is sized for (see score_ctas_per_sm)
@@ -101,5 +114,6 @@ int decode_pages_per_split(long units, int n_pages, int page_size);
 int launch_decode(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int G,
                   int grid_x, int grid_y, cudaStream_t stream);
 int launch_build(const BuildParams& p, int RP, int dtype, int page_size, cudaStream_t stream);
+int launch_append(const AppendParams& p, int batch, cudaStream_t stream);
 
 }  // namespace locks

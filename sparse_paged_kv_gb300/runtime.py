@@ -138,6 +138,19 @@ class LocksLayer:
             self.step()
         return graph
 
+    def append(self, k_new, v_new, completed=None, stream=None):
+        """Write each sequence's new token (k_new, v_new: bf16 [batch][H_kv][d]
+        on the device) at position seq_lens[b], advance seq_lens, and store in
+        `completed` (int32 [batch]) the block of each page the token completed
+        (-1 for none)."""
+        B.locks_append_kv(self.cfg, k_new, v_new, self.k_cache, self.v_cache, self.block_table,
+                          self.seq_lens, completed=completed, status=self.status, stream=stream)
+
+    def build_completed(self, completed, status=None, stream=None):
+        """Summaries of the blocks listed in `completed` (entries < 0 skipped)."""
+        B.locks_build_completed(self.cfg, self.k_cache, completed, self.summaries, status=status,
+                                stream=stream)
+
     # ---- diagnostics ------------------------------------------------------------
     def host_records(self, blocks, h: int):
         """(mu, V, C) of the given physical blocks for KV head h (float64, host)."""
@@ -153,3 +166,49 @@ class LocksLayer:
         c = self.cfg
         return self.torch.full((c.batch, c.n_kv_heads, c.max_pages), float("nan"),
                                dtype=self.torch.float32, device=self.device)
+
+
+class DecodeLoop:
+    """Decode steps of one layer as an engine runs them, with no host round
+    trip: each step appends the new token (current stream), builds the
+    summary of any page that token completed on a side stream, then selects
+    and decodes.  A page completed at step s becomes a selection candidate at
+    step s + 1, so its build overlaps step s's selection and decode, and step
+    s + 1's selection waits for it (section 4 "Build": one build per
+    finalised page, off the critical path).  Two `completed` buffers
+    alternate, so a step's append never overwrites the list the previous
+    step's build may still be reading."""
+
+    def __init__(self, layer: LocksLayer):
+        import torch
+        self.torch = torch
+        self.layer = layer
+        self.side = torch.cuda.Stream(device=layer.device)
+        self.completed = [torch.full((layer.cfg.batch,), -1, dtype=torch.int32,
+                                     device=layer.device) for _ in range(2)]
+        self.appended = torch.cuda.Event()
+        self.built = None             # event: the previous step's build is done
+        self.steps = 0
+
+    def step(self, k_new, v_new, page_lse=None, page_share=None):
+        torch = self.torch
+        L = self.layer
+        cur = torch.cuda.current_stream(L.device)
+        done = self.completed[self.steps & 1]
+        L.append(k_new, v_new, completed=done, stream=cur)
+        self.appended.record(cur)
+        self.side.wait_event(self.appended)
+        L.build_completed(done, stream=self.side)
+        built = torch.cuda.Event()
+        built.record(self.side)
+        if self.built is not None:
+            cur.wait_event(self.built)
+        self.built = built
+        L.select(page_lse=page_lse, page_share=page_share, stream=cur)
+        L.sparse_decode(stream=cur)
+        self.steps += 1
+
+    def finish(self):
+        """Make the current stream wait for the last step's build."""
+        if self.built is not None:
+            self.torch.cuda.current_stream(self.layer.device).wait_event(self.built)

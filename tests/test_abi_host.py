@@ -149,6 +149,32 @@ def test_decode_and_build_validation(lib):
                                      None) == B.LOCKS_ERR_INVALID_ARG
 
 
+def test_append_and_completed_build_validation(lib):
+    """locks_append_kv moves rows as 16-byte words: null or misaligned
+    pointers are refused before any launch; an empty batch does nothing.
+    locks_build_completed validates like locks_build_summaries."""
+    c = cfg()
+    cc = ctypes.byref(c.c())
+    assert lib.locks_append_kv(cc, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+                               None) == B.LOCKS_ERR_INVALID_ARG
+    assert lib.locks_append_kv(cc, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                               None) == B.LOCKS_ERR_INVALID_ARG
+    for i in range(4):
+        args = [FAKE] * 4
+        args[i] = FAKE + 8
+        assert lib.locks_append_kv(cc, *args, FAKE, FAKE, None, None,
+                                   None) == B.LOCKS_ERR_INVALID_ARG, i
+    assert lib.locks_append_kv(ctypes.byref(cfg(batch=0).c()), FAKE, FAKE, FAKE, FAKE, FAKE,
+                               FAKE, None, None, None) == B.LOCKS_OK
+    assert lib.locks_append_kv(ctypes.byref(cfg(page_size=32).c()), FAKE, FAKE, FAKE, FAKE, FAKE,
+                               FAKE, None, None, None) == B.LOCKS_ERR_UNSUPPORTED
+    assert lib.locks_build_completed(cc, FAKE, FAKE, -1, FAKE, None, None, 0,
+                                     None) == B.LOCKS_ERR_INVALID_ARG
+    assert lib.locks_build_completed(cc, FAKE, FAKE, 0, FAKE, None, None, 0, None) == B.LOCKS_OK
+    assert lib.locks_build_completed(cc, FAKE, None, 4, FAKE, None, None, 0,
+                                     None) == B.LOCKS_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, 99):
         assert isinstance(lib.locks_status_string(code), bytes)

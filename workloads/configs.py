@@ -48,6 +48,8 @@ class LocksWorkload:
     seed: int = 1000
     seq_lens: Optional[Tuple[int, ...]] = None   # ragged per-sequence lengths (overrides context)
     spare_blocks: int = 3             # unused physical blocks in the pool (filled with NaN)
+    headroom_pages: int = 0           # block-table entries (and blocks) per sequence beyond its
+                                      # length, for pages a decode loop will start
     description: str = field(default="", compare=False)
 
     # ---- derived sizes -------------------------------------------------
@@ -63,7 +65,8 @@ class LocksWorkload:
 
     @property
     def max_pages(self) -> int:
-        return max(1, max(math.ceil(t / self.page_size) for t in self.lengths()))
+        return max(1, max(math.ceil(t / self.page_size) for t in self.lengths())) + \
+            self.headroom_pages
 
     @property
     def page_budget(self) -> int:
