@@ -417,18 +417,46 @@ def algorithmic_bytes(layer, inputs, selected):
     return select_bytes, decode_bytes, dense_bytes
 
 
+FLUSH_NOTE = "flushed before every timed step (256 MiB write, then a 256 MiB read)"
+
+
+def record_stream_bytes(w, rec_bytes: int) -> int:
+    """Summary-record bytes one step scans (every candidate page of every unit)."""
+    B = w.page_size
+    n = 0
+    for t in w.lengths():
+        pages = -(-t // B)
+        n += max(0, min(pages - 1, t // B) - 1)
+    return n * w.n_kv_heads * rec_bytes
+
+
+def l2_policy(torch, w, rec_bytes: int):
+    """(flush?, note): no flush when the records a step streams are at least
+    twice the L2, so that no step finds the previous one's data there; else an
+    L2 flush before every timed step."""
+    l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0)) or 132 * 2 ** 20
+    rb = record_stream_bytes(w, rec_bytes)
+    if rb >= 2 * l2:
+        return False, (f"inputs larger than L2: every step streams {rb / 1e6:.0f} MB of summary "
+                       f"records (>= 2x the {l2 / 1e6:.0f} MB L2) before its decode; no flush")
+    return True, FLUSH_NOTE
+
+
 class Timer:
-    """Event-timed loops on one stream with an L2 flush before every
-    iteration: write 256 MiB (> the 129 MB L2), then read another 256 MiB so
-    the dirty lines are written back before the timed work."""
+    """Event-timed loops on one stream, with (flush=True) an L2 flush before
+    every iteration: write 256 MiB (> the 129 MB L2), then read another
+    256 MiB so the dirty lines are written back before the timed work."""
 
     def __init__(self, torch, stream, dist):
         self.torch, self.stream, self.dist = torch, stream, dist
         self.flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
         self.flush_rd = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
         self.flush_sink = torch.empty((), dtype=torch.float32, device="cuda")
+        self.enabled = True
 
     def flush_l2(self, i):
+        if not self.enabled:
+            return
         self.flush.fill_(float(i & 7))
         self.torch.sum(self.flush_rd, dim=0, out=self.flush_sink)
 
@@ -479,6 +507,7 @@ def measure_record(layer, inputs, timer, K, Wm, sampler, tag, full, args, world,
     w = inputs.workload
     stream = torch.cuda.current_stream()
     res = {}
+    timer.enabled, res["l2"] = l2_policy(torch, w, layer.rec_bytes)
 
     # ---- summary build (one-time, reported separately) ----
     ids = runtime.complete_page_blocks(inputs.block_table, inputs.seq_lens, w.page_size)
@@ -674,8 +703,13 @@ def measure_decode_loop(layer, w, sampler, tag, reps=3):
 
 
 def measure_dense(layer, inputs, timer, K, Wm, sampler, tag):
+    """The dense decode on the same inputs; it reads the whole K/V cache, so
+    it is flushed like a step only when the cache is under twice the L2."""
     import torch
     stream = torch.cuda.current_stream()
+    w = inputs.workload
+    l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0)) or 132 * 2 ** 20
+    timer.enabled = sum(w.lengths()) * w.n_kv_heads * w.head_dim * 4 < 2 * l2
 
     def dstep(ev):
         if ev:
@@ -694,8 +728,8 @@ def summarise(w, res, peak, world, dense_ms=None):
     dec_us = stats_us(res["dec_ms"])["mean"]
     step_gbs = (select_bytes + decode_bytes) / (step["mean"] / 1e6) / 1e9
     sel_gbs = select_bytes / (sel_us / 1e6) / 1e9
-    out = {"step_us": step, "tokens_per_s": aggregate_tokens_per_s(world, w.batch,
-                                                                     res["step_mean_max_ms"]),
+    out = {"l2": res["l2"], "step_us": step,
+           "tokens_per_s": aggregate_tokens_per_s(world, w.batch, res["step_mean_max_ms"]),
            "select_alone_us": sel_us, "sparse_decode_alone_us": dec_us,
            "select_gbs": sel_gbs, "select_frac": sel_gbs / peak,
            "sparse_decode_gbs": decode_bytes / (dec_us / 1e6) / 1e9,
@@ -811,7 +845,7 @@ def run_gpu(args):
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
                    "context": w.context, "rank": w.rank, "budget_tokens": w.budget_tokens,
                    "summary": args.summary, "kv": "bf16",
-                   "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read)",
+                   "l2": res["l2"],
                    "step": "locks_select + locks_sparse_decode, one layer",
                    "parallelism": f"replicas x{world}"},
         "step_us": main["step_us"],

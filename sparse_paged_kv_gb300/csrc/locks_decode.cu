@@ -29,7 +29,7 @@
 //     bf16 output rows;
 //   * ticketed (every page, lists of unequal length): each split writes its
 //     partial to the workspace and the last split of the unit (atomic ticket)
-//     merges them.
+//     brings all of them into shared memory by bulk copies and merges them.
 #include <algorithm>
 
 #include "locks_common.cuh"
@@ -49,12 +49,6 @@ constexpr int kSlotBytes = 4 * kBoxBytes;                  // K0 K1 V0 V1 (32 Ki
 constexpr int kMaxPagesPerSplit = 256;
 constexpr int kMaxClusterSplits = 16;                      // cluster size limit (non-portable above 8)
 constexpr int kMaxMergeCluster = 4;                        // largest cluster the sparse decode uses
-
-// float max through the integer atomics (ordering of IEEE bit patterns)
-__device__ __forceinline__ void atomicMax_float(float* addr, float v) {
-  if (v >= 0.f) atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
-  else atomicMin(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
-}
 
 // distributed shared memory: the address of the same variable in CTA `rank`
 // of the cluster, and loads from it
@@ -119,6 +113,7 @@ __global__ void __launch_bounds__(kDecThreads)
   float* wstate = reinterpret_cast<float*>(slot_nv + 4 * STAGES);   // [4][2G]
   __shared__ int s_blk[kMaxPagesPerSplit], s_nv[kMaxPagesPerSplit];
   __shared__ int s_is_last;
+  __shared__ uint64_t s_merge_bar;   // the last split's bulk copies of the partials
 
   // set-up that touches no memory a previous kernel may write runs before
   // the dependency wait
@@ -127,6 +122,7 @@ __global__ void __launch_bounds__(kDecThreads)
       mbar_init(full + s, 1);
       mbar_init(empty + s, kConsumerWarps);
     }
+    mbar_init(&s_merge_bar, 1);
     mbar_fence_init();
   }
   if (warp == kConsumerWarps && lane == 0) {
@@ -201,6 +197,7 @@ __global__ void __launch_bounds__(kDecThreads)
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first();   // K/V pages are read once per step
       for (int i = 0; i < nst; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES && !mbar_wait_bounded(empty + s, ((i / STAGES) - 1) & 1)) {
@@ -236,10 +233,10 @@ __global__ void __launch_bounds__(kDecThreads)
             if (t < cnt && s_nv[t] > 0) {
               const int row = (s_blk[t] * p.n_kv_heads + h) * B;
               unsigned char* dst = slot + e * PB * 128;   // rows [PB e, PB e + PB) of each box
-              tma_load_2d(dst, &tmap_k, 0, row, full + s);
-              tma_load_2d(dst + kBoxBytes, &tmap_k, 64, row, full + s);
-              tma_load_2d(dst + 2 * kBoxBytes, &tmap_v, 0, row, full + s);
-              tma_load_2d(dst + 3 * kBoxBytes, &tmap_v, 64, row, full + s);
+              tma_load_2d(dst, &tmap_k, 0, row, full + s, pol);
+              tma_load_2d(dst + kBoxBytes, &tmap_k, 64, row, full + s, pol);
+              tma_load_2d(dst + 2 * kBoxBytes, &tmap_v, 0, row, full + s, pol);
+              tma_load_2d(dst + 3 * kBoxBytes, &tmap_v, 64, row, full + s, pol);
             }
           }
         } else {
@@ -445,34 +442,84 @@ __global__ void __launch_bounds__(kDecThreads)
   __threadfence();
 
   // ---- last split of the unit: merge every split -----------------------------
-  // per-head maximum over the splits first (all loads in parallel) ...
-  __shared__ float s_mmax[8];
-  if (tid < G) s_mmax[tid] = -INFINITY;
-  __syncthreads();
-  for (int t = tid; t < nsplits * G; t += kDecThreads) {
-    const int s2 = t / G, gg = t % G;
-    const float m2 = __ldcg(p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + gg) * part_stride);
-    if (m2 != -INFINITY) atomicMax_float(s_mmax + gg, m2);
+  // The unit's partials (nsplits x G x kPartStride floats) are contiguous in
+  // the workspace: they come into the idle ring by one bulk copy per chunk of
+  // as many splits as it holds, so every load is in flight at once; each
+  // thread merges its output entries' (m, l, acc) from shared memory, per
+  // chunk by its maximum first, then into a running state.
+  constexpr int kItems = (G * 32 + kDecThreads - 1) / kDecThreads;
+  const uint32_t split_bytes = uint32_t(G * part_stride * sizeof(float));
+  const int cap = int((size_t(STAGES) * kSlotBytes) / split_bytes);
+  const float* src = p.ws_part + size_t(u) * p.n_splits_max * G * part_stride;
+  const float* buf = reinterpret_cast<const float*>(ring);
+  float rM[kItems], rL[kItems];
+  float4 rA[kItems];
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    rM[it] = -INFINITY;
+    rL[it] = 0.f;
+    rA[it] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  __syncthreads();
-  // ... then the rescaled sums, whose loads no longer depend on each other
-  for (int t = tid; t < G * 32; t += kDecThreads) {
-    const int gg = t >> 5, l4 = t & 31;
-    const float M = s_mmax[gg];
-    float L = 0.f;
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-#pragma unroll 8
-      for (int s2 = 0; s2 < nsplits; ++s2) {
-        const float* pg = p.ws_part + ((size_t(u) * p.n_splits_max + s2) * G + gg) * part_stride;
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg));
-        const float4 a2 = __ldcg(reinterpret_cast<const float4*>(pg + 4 + 4 * l4));
-        const float f = ml.x == -INFINITY ? 0.f : exp2f((ml.x - M) * p.scale_log2);
-        L += ml.y * f;
-        A.x += a2.x * f; A.y += a2.y * f; A.z += a2.z * f; A.w += a2.w * f;
-      }
+  bool merge_ok = true;
+  int ph = 0;
+  for (int c0 = 0; c0 < nsplits && merge_ok; c0 += cap, ++ph) {
+    const int cn = min(cap, nsplits - c0);
+    if (tid == 0) {
+      // the other splits' partials were written through the generic proxy (and
+      // made visible by their fences and the ticket); order them, and this
+      // CTA's earlier use of the ring, before the copy engine's accesses
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(&s_merge_bar, uint32_t(cn) * split_bytes);
+      bulk_g2s(ring, src + size_t(c0) * G * part_stride, uint32_t(cn) * split_bytes, &s_merge_bar);
     }
-    store_out_row(p, b, h, G, gg, l4, A, L, M);
+    // every thread waits; the block agrees on the outcome before any leaves
+    const bool landed = mbar_wait_bounded(&s_merge_bar, ph & 1);
+    if (__syncthreads_or(!landed)) {
+      if (tid == 0) flag_status(p.status, LOCKS_DEV_WAIT_TIMEOUT);
+      merge_ok = false;
+      break;
+    }
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int t = tid + it * kDecThreads;
+      if (t >= G * 32) break;
+      const int gg = t >> 5, l4 = t & 31;
+      float Mc = -INFINITY;
+      for (int s2 = 0; s2 < cn; ++s2) Mc = fmaxf(Mc, buf[(s2 * G + gg) * part_stride]);
+      if (Mc == -INFINITY) continue;
+      float Lc = 0.f;
+      float4 Ac = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int s2 = 0; s2 < cn; ++s2) {
+        const float* pg = buf + (s2 * G + gg) * part_stride;
+        const float2 ml = *reinterpret_cast<const float2*>(pg);
+        const float4 a2 = *reinterpret_cast<const float4*>(pg + 4 + 4 * l4);
+        const float f = ml.x == -INFINITY ? 0.f : exp2f((ml.x - Mc) * p.scale_log2);
+        Lc += ml.y * f;
+        Ac.x += a2.x * f; Ac.y += a2.y * f; Ac.z += a2.z * f; Ac.w += a2.w * f;
+      }
+      const float Mn = fmaxf(rM[it], Mc);
+      const float fo = rM[it] == -INFINITY ? 0.f : exp2f((rM[it] - Mn) * p.scale_log2);
+      const float fc = exp2f((Mc - Mn) * p.scale_log2);
+      rL[it] = rL[it] * fo + Lc * fc;
+      rA[it].x = rA[it].x * fo + Ac.x * fc;
+      rA[it].y = rA[it].y * fo + Ac.y * fc;
+      rA[it].z = rA[it].z * fo + Ac.z * fc;
+      rA[it].w = rA[it].w * fo + Ac.w * fc;
+      rM[it] = Mn;
+    }
+    __syncthreads();                               // the next chunk overwrites the ring
+  }
+  if (!merge_ok) {
+    // let the copy in flight land before the CTA can exit
+    mbar_wait_bounded(&s_merge_bar, ph & 1);
+  } else {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int t = tid + it * kDecThreads;
+      if (t < G * 32) store_out_row(p, b, h, G, t >> 5, t & 31, rA[it], rL[it], rM[it]);
+    }
   }
   if (tid == 0) p.ws_ticket[u] = 0;
 }

@@ -154,6 +154,17 @@ __device__ __forceinline__ void load_qfrag(QFrag& f, const __nv_bfloat16* qh, in
                         __uint_as_float(raw[s][h] & 0xffff0000u) * down);
 }
 
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  unsigned long long ra, rb, rd;
+  ra = *reinterpret_cast<unsigned long long*>(&a);
+  rb = *reinterpret_cast<unsigned long long*>(&b);
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  return *reinterpret_cast<float2*>(&rd);
+}
+__device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
+  return make_float2(__shfl_xor_sync(kFull, v.x, o), __shfl_xor_sync(kFull, v.y, o));
+}
+
 // Scores the two quantised page summaries of a slot pair (records r0 and
 // r0 + rec_bytes) with the whole warp; pb is the warp's [2][17][8] pair
 // buffer.  Returns, in lane 16 * p + hl, s_hat of page p and head hl / (16/G).
@@ -297,23 +308,22 @@ __device__ __forceinline__ float score_pair_i4(const unsigned char* r0, uint32_t
   // accumulator d, lane 4g+t: tokens 16m+g (elements 0, 1) and 16m+g+8 (2, 3)
   // of columns 2t, 2t+1; packed, column c is head c % 4 of page c / 4
   const float cu = qf.pw * scale_log2;
+  const float2 cu2 = make_float2(cu, cu);
   float res[NSET][2];
 #pragma unroll
   for (int d = 0; d < NSET; ++d) {
     const int page = kPack ? (t >> 1) : d;
     const unsigned char* rb = r0 + page * rec_bytes;
     const float* cs = reinterpret_cast<const float*>(rb + i4_cscale(RP, PB));
-    float z[MT][4];
+    float2 z[MT][2];
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       const float s0 = cs[16 * m + g], s1 = cs[16 * m + g + 8];
-      z[m][0] = acc[d][m][0] * s0;
-      z[m][1] = acc[d][m][1] * s0;
-      z[m][2] = acc[d][m][2] * s1;
-      z[m][3] = acc[d][m][3] * s1;
-      mx0 = fmaxf(mx0, fmaxf(z[m][0], z[m][2]));
-      mx1 = fmaxf(mx1, fmaxf(z[m][1], z[m][3]));
+      z[m][0] = fmul2(make_float2(acc[d][m][0], acc[d][m][1]), make_float2(s0, s0));
+      z[m][1] = fmul2(make_float2(acc[d][m][2], acc[d][m][3]), make_float2(s1, s1));
+      mx0 = fmaxf(mx0, fmaxf(z[m][0].x, z[m][1].x));
+      mx1 = fmaxf(mx1, fmaxf(z[m][0].y, z[m][1].y));
     }
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -321,17 +331,18 @@ __device__ __forceinline__ float score_pair_i4(const unsigned char* r0, uint32_t
       mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
     }
     const float mc0 = mx0 * cu, mc1 = mx1 * cu;
-    float e0 = 0.f, e1 = 0.f;
+    const float2 nmc = make_float2(-mc0, -mc1);
+    float2 e = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      e0 += ex2_approx(fmaf(z[m][0], cu, -mc0)) + ex2_approx(fmaf(z[m][2], cu, -mc0));
-      e1 += ex2_approx(fmaf(z[m][1], cu, -mc1)) + ex2_approx(fmaf(z[m][3], cu, -mc1));
-    }
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      e0 += __shfl_xor_sync(kFull, e0, o);
-      e1 += __shfl_xor_sync(kFull, e1, o);
-    }
+      for (int r = 0; r < 2; ++r) {
+        const float2 x = ffma2(z[m][r], cu2, nmc);
+        e = fadd2(e, make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+      }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) e = fadd2(e, shfl_xor2(e, o));
+    const float e0 = e.x, e1 = e.y;
     const float2 a = *reinterpret_cast<const float2*>(pb + page * kPS + 128 +
                                                       (kPack ? 2 * (t & 1) : 2 * t));
     const float sa = scale * qf.pw;
@@ -505,12 +516,13 @@ __global__ void __launch_bounds__(kSelThreads, (!std::is_same_v<T, I4Rec> &&
     const uint32_t bytes = uint32_t(rec_bytes) * ((b0 >= 0) + (b1 >= 0));
     if (bytes) {
       mbar_arrive_expect_tx(mybar + s, bytes);
+      const uint64_t pol = l2_evict_first();
       if (b0 >= 0)
-        bulk_g2s(myring + size_t(2 * s) * rec_bytes, sum_base + size_t(b0) * rec_bytes,
-                 uint32_t(rec_bytes), mybar + s);
+        bulk_g2s_hint(myring + size_t(2 * s) * rec_bytes, sum_base + size_t(b0) * rec_bytes,
+                      uint32_t(rec_bytes), mybar + s, pol);
       if (b1 >= 0)
-        bulk_g2s(myring + size_t(2 * s + 1) * rec_bytes, sum_base + size_t(b1) * rec_bytes,
-                 uint32_t(rec_bytes), mybar + s);
+        bulk_g2s_hint(myring + size_t(2 * s + 1) * rec_bytes, sum_base + size_t(b1) * rec_bytes,
+                      uint32_t(rec_bytes), mybar + s, pol);
     } else {
       mbar_arrive(mybar + s);
     }

@@ -117,24 +117,30 @@ __device__ __forceinline__ void block_emit_topk(const uint32_t* keys, int m, uin
   }
 }
 
+// Rank of key `mine` (at index `me`) among keys[0..m): how many are larger,
+// or equal at a smaller index.  A plain loop: this code runs once per step,
+// usually from a cold instruction cache, where a short loop beats an
+// unrolled one.
+__device__ __forceinline__ int rank_in(const uint32_t* keys, int m, uint32_t mine, int me) {
+  int r = 0;
+  for (int j = 0; j < m; ++j) {
+    const uint32_t o = keys[j];
+    r += (o > mine || (o == mine && j < me)) ? 1 : 0;
+  }
+  return r;
+}
+
 // Calls put(i, pos) for the K largest (1 <= K < m <= kFinThreads) of the keys
-// keys[0..m) -- ordered by key, then by smaller index -- in index order:
-// thread i ranks key i against all m keys directly, one scan places the
-// winners.  For short lists this beats bounding and compacting first.
+// keys[0..m) -- ordered by key, then by smaller index -- in
+// index order: thread i ranks key i against all m keys directly, one scan
+// places the winners.  For short lists this beats bounding and compacting
+// first.
 template <typename F>
 __device__ __forceinline__ void block_topk_small(const uint32_t* keys, int m, int K, int* s_warp,
                                                  F&& put) {
   const int tid = threadIdx.x;
   bool win = false;
-  if (tid < m) {
-    const uint32_t mine = keys[tid];
-    int r = 0;
-    for (int j = 0; j < m; ++j) {
-      const uint32_t o = keys[j];
-      r += (o > mine || (o == mine && j < tid)) ? 1 : 0;
-    }
-    win = r < K;
-  }
+  if (tid < m) win = rank_in(keys, m, keys[tid], tid) < K;
   const int pos = block_excl_scan(win ? 1 : 0, s_warp);
   if (win) put(tid, pos);
 }
@@ -142,10 +148,10 @@ __device__ __forceinline__ void block_topk_small(const uint32_t* keys, int m, in
 constexpr int kSurvCap = 1024;               // survivors the ranking path holds
 
 // Shared-memory scratch of block_topk.
-struct TopkScratch {
-  uint32_t wj[kFinWarps];                    // per warp: its j-th largest thread maximum
-  uint32_t sk[kSurvCap];                     // survivors: key
+struct alignas(16) TopkScratch {
+  uint32_t sk[kSurvCap];                     // survivors: key (16-byte aligned)
   int si[kSurvCap];                          //            index
+  uint32_t wj[kFinWarps];                    // per warp: its j-th largest thread maximum
   int scan[6][kFinWarps];
 };
 
@@ -219,13 +225,7 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int m, int K, T
   uint32_t win = 0u;                           // bit q: survivor j0 + q wins (ps <= 4)
   int nw = 0;
   for (int j = j0; j < j1; ++j) {
-    const uint32_t kj = S.sk[j];
-    int r = 0;
-    for (int q = 0; q < n_surv; ++q) {
-      const uint32_t o = S.sk[q];
-      r += (o > kj || (o == kj && q < j)) ? 1 : 0;
-    }
-    if (r < K) { win |= 1u << (j - j0); ++nw; }
+    if (rank_in(S.sk, n_surv, S.sk[j], j) < K) { win |= 1u << (j - j0); ++nw; }
   }
   const int pos0 = block_excl_scan(nw, S.scan[4]);
   int pos = pos0;

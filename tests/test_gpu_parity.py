@@ -56,6 +56,12 @@ CASES = {
     "b16_gqa4_k128": TINY.with_(page_size=16, batch=2, n_q_heads=32, n_kv_heads=8,
                                 context=16384, budget_tokens=2048, global_rank=16,
                                 carrier_count=None, carrier_frac=0.01, seed=2024),
+    # 16 KV heads (G = 2)
+    "heads16": TINY.with_(n_q_heads=32, n_kv_heads=16, context=64 * 40 + 9, seed=2040),
+    # ragged sequences of several lengths sharing score CTAs, 8 KV heads
+    "ragged_8heads": TINY.with_(batch=6, n_q_heads=32, n_kv_heads=8,
+                              seq_lens=(64 * 200 + 3, 64 * 3, 64 * 57, 0, 64 * 130 - 1, 64 * 2 + 1),
+                              global_rank=16, seed=2041),
 }
 
 
@@ -97,8 +103,9 @@ def test_parity_bf16_records(name):
           f"{rep.max_record_err:.2e} ties {rep.tie_diffs}")
 
 
-I4_CASES = ["tiny", "ragged", "group8", "rank16", "rank3", "multichunk", "slices3", "k40", "b16",
-            "b16_ragged", "cluster_merge"]
+I4_CASES = ["tiny", "ragged", "group1", "group2", "group8", "rank16", "rank3", "multichunk",
+            "slices3", "k40", "b16", "b16_ragged", "b16_rank15", "cluster_merge", "batch_heads",
+            "group8_k40_slices3", "heads16", "ragged_8heads", "b16_gqa4_k128"]
 
 
 @pytest.mark.parametrize("name", I4_CASES)
