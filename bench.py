@@ -237,6 +237,21 @@ def build_flop_count(sweeps, B: int, d_head: int = 128, r: int = 8) -> float:
     return float(sweeps.size * fixed + sweeps.sum() * per_sweep + (sweeps + 1).sum() * 2 * B * B)
 
 
+def trd_flop_count(n_page_heads: int, B: int, d_head: int = 128, r: int = 8, rounds: int = 6,
+                   iters: int = 2) -> float:
+    """Floating-point operations of the tridiagonal top-r build per page-heads:
+    centring (B d), the Gram (2 B^2 d), the Householder reduction (a
+    matrix-vector product and a rank-2 update of the trailing m x m block per
+    step, 6 m^2, about 2 B^3 in all), the bisection (r eigenvalues x rounds x
+    16 Sturm counts of B steps, 4 flops each), inverse iteration (r x iters x
+    B x 12), the Rayleigh quotients (6 r B), the back-transformation (4 m per
+    vector and step, about 2 r B^2) and the basis V = D^T U_r (2 d B r)."""
+    tri = sum(6 * m * m for m in range(2, B))
+    per = (B * d_head + 2 * B * B * d_head + tri + r * rounds * 16 * B * 4 + r * iters * B * 12 +
+           6 * r * B + 2 * r * B * B + 2 * d_head * B * r)
+    return float(n_page_heads) * per
+
+
 def captured_energy(layer, ids_t, tail, w, sample: int = 4096):
     """Energy the rank-r summary captures per page-head, 1 - tau / ||D||_F^2
     (a diagnostic the paper reports for real pages, App. D): tau is the build's
@@ -527,8 +542,11 @@ def measure_record(layer, inputs, timer, K, Wm, sampler, tag, full, args, world,
     build_ms = min(build_ms)
     page_heads = len(ids) * w.n_kv_heads
     bstat_np = bstat.cpu().numpy()
-    build_flops = build_flop_count(bstat_np & 0xFFFF, w.page_size, r=w.rank)
-    res["build"] = {"ms": build_ms, "page_heads": page_heads,
+    trd = w.page_size == 64            # the default solver at B = 64 (no sweep cap passed)
+    build_flops = (trd_flop_count(bstat_np.size, w.page_size, r=w.rank) if trd
+                   else build_flop_count(bstat_np & 0xFFFF, w.page_size, r=w.rank))
+    res["build"] = {"solver": "tridiagonal (Householder, bisection, inverse iteration)" if trd
+                    else "cyclic Jacobi", "ms": build_ms, "page_heads": page_heads,
                     "pages_per_s": len(ids) / (build_ms / 1e3),
                     "page_heads_per_s": page_heads / (build_ms / 1e3),
                     "not_converged": int(((bstat_np >> 16) != 0).sum()),
@@ -645,7 +663,7 @@ def measure_record(layer, inputs, timer, K, Wm, sampler, tag, full, args, world,
     return res
 
 
-def measure_decode_loop(layer, w, sampler, tag, reps=3):
+def measure_decode_loop(layer, w, sampler, tag, reps=5):
     """B consecutive decode-loop steps (locks_append_kv, locks_build_completed
     on a side stream, select, sparse decode) starting from length T - B, so
     the last step completes one page per sequence and its build runs as it
@@ -654,6 +672,7 @@ def measure_decode_loop(layer, w, sampler, tag, reps=3):
     difference per step is the amortised cost of appending and of the
     page-crossing refresh.  The appended rows overwrite the last page's keys
     and values with new random ones; lengths end where they started."""
+    import numpy as np
     import torch
     from sparse_paged_kv_gb300 import runtime
     B = w.page_size
@@ -673,9 +692,11 @@ def measure_decode_loop(layer, w, sampler, tag, reps=3):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
+    host_lens = np.asarray(layer.host_seq_lens, dtype=np.int64)
+
     def looped():
         layer.seq_lens.copy_(lens0 - B)
-        loop = runtime.DecodeLoop(layer)
+        loop = runtime.DecodeLoop(layer, host_lengths=host_lens - B)
         torch.cuda.synchronize()
         e0.record(stream)
         for s in range(B):
@@ -698,8 +719,9 @@ def measure_decode_loop(layer, w, sampler, tag, reps=3):
     return {"steps": B, "runs": reps, "plain_us_per_step": p_us, "loop_us_per_step": l_us,
             "refresh_us_per_step": l_us - p_us, "refresh_fraction_of_step": (l_us - p_us) / p_us,
             "pages_completed_per_run": int((done >= 0).sum()), "completions_as_expected": ok,
-            "note": "B consecutive steps, no L2 flush: append + build of the completed pages "
-                    "on a side stream + select + sparse decode, against select + sparse decode"}
+            "note": "B consecutive steps, no L2 flush: append + (on the step that completes a "
+                    "page) its build on a side stream + select + sparse decode, against select + "
+                    "sparse decode"}
 
 
 def measure_dense(layer, inputs, timer, K, Wm, sampler, tag):

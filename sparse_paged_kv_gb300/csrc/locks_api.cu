@@ -163,6 +163,7 @@ int build_common(const locks_cfg_t* cfg, const void* k_cache, const int32_t* blo
   p.num_blocks = cfg->num_blocks;
   p.rank = cfg->rank;
   p.max_sweeps = max_sweeps == 0 ? 20 : max_sweeps;
+  p.use_trd = max_sweeps == 0 && cfg->page_size == 64;   // a sweep cap asks for Jacobi
   p.skip_negative = skip_negative;
   return locks::launch_build(p, locks::rank_cap(cfg->rank), cfg->summary_dtype, cfg->page_size,
                              static_cast<cudaStream_t>(stream));

@@ -15,6 +15,7 @@
 //      coefficients); V = D^T U_r S_r^-1, C = U_r S_r,
 //      tau = sum of the remaining eigenvalues;
 //   5. the record (mu, V, C) in the layout locks_select reads.
+#include <cfloat>
 #include <cstddef>
 #include <type_traits>
 
@@ -50,6 +51,18 @@ struct BuildSmem {
   float tau;
   int flag;
   unsigned char lp[PB - 1][PB / 2], lq[PB - 1][PB / 2];   // round labels (below)
+  // the tridiagonal solver's scratch (B = 64 only)
+  static constexpr int kTrd = PB == 64 ? 1 : 0;
+  struct Trd {
+    float d[PB], e[PB], e2[PB], tau[PB];  // T = Q^T A Q (diagonal, subdiagonal, its
+                                          // squares); Householder scalars
+    float v[PB], w[PB];                   // the current reflection's v and w
+    float pp[4][PB];                      // partial products S v of the row groups
+    float yc[PB][16], yz[PB][16];         // inverse iteration: the Thomas recurrences
+    float sigma[16], lamr[16];            // shifts; Rayleigh quotients
+    int clus[16];                         // cluster of each wanted eigenvalue
+    float lo, hi, pivmin, tpiv, trace;
+  } trd[kTrd];
 
   __device__ float* D() { return work; }             // [B][kDS]: steps 1-2
   __device__ float* A() { return work; }             // [B][AS]: steps 2-4
@@ -157,30 +170,41 @@ __device__ __forceinline__ uint32_t quant_biased(float x, float scale, int qmax)
   return uint32_t(int(c) + qmax + 1);
 }
 
+// v[k] = sum_i (key_i[t] - mu_t) U[i][order[k]] over the page's tokens: the
+// unnormalised basis entries of dimension t for the modes k < r (modes past
+// the rank read column 0 and are discarded by the caller).  The mode indices
+// are read once; every token's row of U is a broadcast read.
+template <int RP, int PB, int kAS, typename Smem>
+__device__ __forceinline__ void basis_column_sums(const Smem& S, const __nv_bfloat16* kp, int t,
+                                                  float mu_t, int r, float (&v)[RP]) {
+  int ord[RP];
+#pragma unroll
+  for (int k = 0; k < RP; ++k) {
+    ord[k] = k < r ? S.order[k] : 0;
+    v[k] = 0.f;
+  }
+  const float* U = const_cast<Smem&>(S).U();
+#pragma unroll 4
+  for (int i = 0; i < PB; ++i) {
+    const float dit = __bfloat162float(kp[i * kHeadDim + t]) - mu_t;
+    const float* urow = U + i * kAS;
+#pragma unroll
+    for (int k = 0; k < RP; ++k) v[k] = fmaf(dit, urow[ord[k]], v[k]);
+  }
+}
+
 template <int RP, int PB, typename Smem>
 __device__ __forceinline__ void write_i4_record(Smem& S, const BuildParams& prm, int blk, int h,
-                                                int r) {
+                                                int r, const __nv_bfloat16* kp) {
   constexpr int kAS = Smem::AS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned char* rb = static_cast<unsigned char*>(prm.summaries) +
                       (size_t(blk) * prm.n_kv_heads + h) * prm.rec_bytes;
   const float* U = S.U();
   // basis values v_k[t] (as the float record stores them), D re-formed from
-  // the key page as step 1 formed it
+  // the key page kp as step 1 formed it
   float v[RP];
-  if (tid < kHeadDim) {
-    const __nv_bfloat16* kp = prm.k_cache + (size_t(blk) * prm.n_kv_heads + h) * (PB * kHeadDim);
-    const float mu_t = S.mu[tid];
-#pragma unroll
-    for (int k = 0; k < RP; ++k) v[k] = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < PB; ++i) {
-      const float dit = __bfloat162float(kp[i * kHeadDim + tid]) - mu_t;
-#pragma unroll
-      for (int k = 0; k < RP; ++k)
-        if (k < r) v[k] += dit * U[i * kAS + S.order[k]];
-    }
-  }
+  if (tid < kHeadDim) basis_column_sums<RP, PB, kAS>(S, kp, tid, S.mu[tid], r, v);
   __syncthreads();
   float* Vs = S.Vs();                                      // [RP][d]
   if (tid < kHeadDim) {
@@ -265,7 +289,276 @@ __device__ __forceinline__ void write_i4_record(Smem& S, const BuildParams& prm,
   }
 }
 
-template <int RP, typename T, int PB>
+// ---- top-r eigenpairs of the B x B Gram by tridiagonalisation (B = 64) ----
+//   1. A = Q T Q^T, T tridiagonal, by B-2 Householder reflections (the
+//      unblocked symmetric reduction: each step forms v from the column below
+//      the diagonal, p = tau S v, w = p - (tau/2)(p.v) v and S -= v w^T + w v^T
+//      on the trailing block S); v_k stays in A's column k below the diagonal;
+//   2. the r largest eigenvalues of T, each bracketed by six rounds of
+//      16-way multisection with Sturm counts (a half-warp per eigenvalue,
+//      one count per lane): 24 bits of the Gershgorin interval;
+//   3. their eigenvectors by two steps of inverse iteration with the bracket's
+//      midpoint as shift (tridiagonal elimination, pivots kept off zero),
+//      orthonormalised in order within clusters of equal eigenvalues; the
+//      eigenvalues are then the Rayleigh quotients y^T T y;
+//   4. U = Q Y by applying the reflections in reverse order.
+// Leaves the eigenvectors as columns 0..r-1 of U (in descending eigenvalue
+// order), lam[k] (0 for a dropped mode), order[k] = k and tau.
+constexpr int kTrdRounds = 6;
+constexpr int kTrdIters = 2;
+constexpr float kTrdCluster = 1e-5f;   // relative gap below which eigenvalues are one cluster
+
+__device__ __forceinline__ float trd_start(int i, int j) {
+  // a fixed, data-independent start vector for inverse iteration
+  uint32_t h = uint32_t(i) * 2654435761u + uint32_t(j) * 40503u + 12345u;
+  h = (h ^ (h >> 15)) * 2246822519u;
+  return float((h >> 8) & 0xffffu) * (1.f / 65536.f) - 0.5f;
+}
+
+template <int PB, typename Smem>
+__device__ void trd_top_r(Smem& S, int r) {
+  static_assert(PB == 64, "the tridiagonal solver is laid out for 64 x 64 Grams");
+  constexpr int kAS = Smem::AS;
+  constexpr int n = PB;
+  auto& tr = S.trd[0];
+  float* const A = S.A();
+  float* const U = S.U();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // ---- 1. Householder tridiagonalisation -----------------------------------
+  // Every warp forms the step's reflection itself from the column below the
+  // diagonal (no barrier between that and the matrix-vector product);
+  // v_i = x_i / (x_0 - beta) is formed where it is used, and warp 0 stores
+  // it in the column once the trailing block is updated.
+  for (int k = 0; k < n - 2; ++k) {
+    const int m = n - 1 - k;                  // rows k+1 .. n-1
+    float* col = A + (k + 1) * kAS + k;       // col[i * kAS] = A[k+1+i][k]
+    const float x0 = col[0];
+    float sq = 0.f;
+    for (int i = 1 + lane; i < m; i += 32) { const float x = col[i * kAS]; sq += x * x; }
+    sq = group_sum<32>(sq);
+    if (sq == 0.f) {                          // the column is already reduced
+      if (tid == 0) { tr.tau[k] = 0.f; tr.e[k] = x0; }
+      continue;                               // block-uniform: every warp saw the same column
+    }
+    const float beta = -copysignf(sqrtf(x0 * x0 + sq), x0);
+    const float tau = (beta - x0) / beta;
+    const float scale = 1.f / (x0 - beta);
+    auto vv = [&](int i) { return i == 0 ? 1.f : col[i * kAS] * scale; };
+    {
+      // p = tau S v: thread (column i, row group g) sums rows j = g mod 4
+      const int i = tid & (n - 1), g = tid >> 6;
+      float acc = 0.f;
+      if (i < m) {
+#pragma unroll 4
+        for (int j = g; j < m; j += 4) acc += A[(k + 1 + j) * kAS + k + 1 + i] * vv(j);
+      }
+      tr.pp[g][i] = acc;
+      if (tid < m) tr.v[tid] = vv(tid);
+    }
+    __syncthreads();
+    {
+      // K = -(tau / 2) p.v (every warp), w = p + K v (rows 8 warp .. 8 warp + 7)
+      float pv = 0.f;
+      for (int i = lane; i < m; i += 32)
+        pv += tau * (tr.pp[0][i] + tr.pp[1][i] + tr.pp[2][i] + tr.pp[3][i]) * tr.v[i];
+      pv = group_sum<32>(pv);
+      const float K = -0.5f * tau * pv;
+      const int i = warp * (n / 8) + lane;
+      if (lane < n / 8 && i < m)
+        tr.w[i] = tau * (tr.pp[0][i] + tr.pp[1][i] + tr.pp[2][i] + tr.pp[3][i]) + K * tr.v[i];
+    }
+    __syncthreads();
+    {
+      // S -= v w^T + w v^T: thread column j, rows i = g mod 4
+      const int j = tid & (n - 1);
+      if (j < m) {
+        const float vj = tr.v[j], wj = tr.w[j];
+#pragma unroll 4
+        for (int i = tid >> 6; i < m; i += 4)
+          A[(k + 1 + i) * kAS + k + 1 + j] -= tr.v[i] * wj + tr.w[i] * vj;
+      }
+      // the reflection, kept in the reduced column for step 4
+      if (warp == 0) {
+        for (int i = 1 + lane; i < m; i += 32) col[i * kAS] = tr.v[i];
+        if (lane == 0) { tr.tau[k] = tau; tr.e[k] = beta; }
+      }
+    }
+    __syncthreads();
+  }
+  if (tid < n) tr.d[tid] = A[tid * kAS + tid];
+  if (tid == 0) { tr.e[n - 2] = A[(n - 1) * kAS + n - 2]; tr.e[n - 1] = 0.f; }
+  __syncthreads();
+
+  // ---- 2. the r largest eigenvalues of T -------------------------------------
+  if (warp == 0) {
+    float lo = INFINITY, hi = -INFINITY, emax = 0.f, tr_sum = 0.f;
+    for (int i = lane; i < n; i += 32) {
+      const float ei = tr.e[i], em = i > 0 ? tr.e[i - 1] : 0.f;
+      const float rad = fabsf(em) + fabsf(ei);
+      lo = fminf(lo, tr.d[i] - rad);
+      hi = fmaxf(hi, tr.d[i] + rad);
+      emax = fmaxf(emax, ei * ei);
+      tr_sum += tr.d[i];
+      tr.e2[i] = ei * ei;
+    }
+    lo = -group_max<32>(-lo);
+    hi = group_max<32>(hi);
+    emax = group_max<32>(emax);
+    tr_sum = group_sum<32>(tr_sum);
+    if (lane == 0) {
+      tr.lo = lo;
+      tr.hi = hi;
+      tr.pivmin = FLT_MIN * fmaxf(1.f, emax);
+      tr.tpiv = fmaxf(FLT_MIN, 1.2e-7f * fmaxf(fabsf(lo), fabsf(hi)));
+      tr.trace = tr_sum;
+    }
+  }
+  __syncthreads();
+  {
+    // half-warp hw brackets eigenvalue hw from the top; lane hl counts the
+    // eigenvalues below point hl + 1 of 16 (the points rise with hl, so the
+    // lanes whose count is at most idx form a prefix)
+    const int hw = tid >> 4, hl = tid & 15;
+    if (2 * warp < r) {                       // both halves of the warp take part
+      const int idx = n - 1 - min(hw, r - 1);
+      const float pivmin = tr.pivmin;
+      float a = tr.lo, b = tr.hi;
+      for (int round = 0; round < kTrdRounds; ++round) {
+        const float x = a + (b - a) * float(hl + 1) * (1.f / 16.f);
+        float q = tr.d[0] - x;
+        if (fabsf(q) < pivmin) q = -pivmin;
+        int c = q < 0.f;
+        for (int i = 1; i < n; ++i) {
+          q = tr.d[i] - x - __fdividef(tr.e2[i - 1], q);
+          if (fabsf(q) < pivmin) q = -pivmin;
+          c += q < 0.f;
+        }
+        const unsigned le = (__ballot_sync(kFull, c <= idx) >> (lane & 16)) & 0xffffu;
+        const int nle = __popc(le);
+        const float a2 = a + (b - a) * float(nle) * (1.f / 16.f);
+        const float b2 = a + (b - a) * float(nle + 1) * (1.f / 16.f);
+        a = a2;
+        b = b2;
+      }
+      if (hl == 0 && hw < r) tr.sigma[hw] = 0.5f * (a + b);
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. eigenvectors of T by inverse iteration (warp 0, lane j) -----------
+  if (warp == 0) {
+    if (lane == 0) {
+      const float tol = kTrdCluster * fmaxf(fabsf(tr.lo), fabsf(tr.hi));
+      tr.clus[0] = 0;
+      for (int j = 1; j < r; ++j) tr.clus[j] = (tr.sigma[j - 1] - tr.sigma[j]) < tol ? tr.clus[j - 1] : j;
+    }
+    if (lane < r)
+      for (int i = 0; i < n; ++i) U[i * kAS + lane] = trd_start(i, lane);
+    __syncwarp();
+    const float tpiv = tr.tpiv;
+    for (int it = 0; it < kTrdIters; ++it) {
+      if (lane < r) {
+        const int j = lane;
+        const float sg = tr.sigma[j];
+        float cp = 0.f, zp = 0.f;
+        for (int i = 0; i < n; ++i) {
+          const float em = i > 0 ? tr.e[i - 1] : 0.f;
+          float piv = tr.d[i] - sg - em * cp;
+          if (fabsf(piv) < tpiv) piv = piv < 0.f ? -tpiv : tpiv;
+          const float inv = __fdividef(1.f, piv);
+          cp = tr.e[i] * inv;
+          zp = (U[i * kAS + j] - em * zp) * inv;
+          tr.yc[i][j] = cp;
+          tr.yz[i][j] = zp;
+        }
+        float x = tr.yz[n - 1][j], nrm = x * x;
+        U[(n - 1) * kAS + j] = x;
+        for (int i = n - 2; i >= 0; --i) {
+          x = tr.yz[i][j] - tr.yc[i][j] * x;
+          U[i * kAS + j] = x;
+          nrm += x * x;
+        }
+        const bool ok = nrm > 0.f && nrm < INFINITY;
+        const float sc = ok ? rsqrtf(nrm) : 0.f;
+        for (int i = 0; i < n; ++i) U[i * kAS + j] = ok ? U[i * kAS + j] * sc : (i == j ? 1.f : 0.f);
+      }
+      __syncwarp();
+      // Gram-Schmidt within clusters, in eigenvalue order (lanes over rows)
+      for (int j = 1; j < r; ++j) {
+        bool touched = false;
+        for (int a = 0; a < j; ++a) {
+          if (tr.clus[a] != tr.clus[j]) continue;
+          float dt = U[lane * kAS + a] * U[lane * kAS + j] +
+                     U[(lane + 32) * kAS + a] * U[(lane + 32) * kAS + j];
+          dt = group_sum<32>(dt);
+          U[lane * kAS + j] -= dt * U[lane * kAS + a];
+          U[(lane + 32) * kAS + j] -= dt * U[(lane + 32) * kAS + a];
+          touched = true;
+          __syncwarp();
+        }
+        if (touched) {
+          float nn = U[lane * kAS + j] * U[lane * kAS + j] +
+                     U[(lane + 32) * kAS + j] * U[(lane + 32) * kAS + j];
+          nn = group_sum<32>(nn);
+          const float sc = nn > 0.f ? rsqrtf(nn) : 0.f;
+          U[lane * kAS + j] *= sc;
+          U[(lane + 32) * kAS + j] *= sc;
+          __syncwarp();
+        }
+      }
+    }
+    // Rayleigh quotients y^T T y
+    if (lane < r) {
+      const int j = lane;
+      float acc = 0.f;
+      for (int i = 0; i < n; ++i) {
+        const float yi = U[i * kAS + j];
+        float t = tr.d[i] * yi;
+        if (i > 0) t += tr.e[i - 1] * U[(i - 1) * kAS + j];
+        if (i < n - 1) t += tr.e[i] * U[(i + 1) * kAS + j];
+        acc += yi * t;
+      }
+      tr.lamr[j] = acc;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const float lam1 = tr.lamr[0];
+      float top = 0.f;
+      for (int k = 0; k < r; ++k) {
+        const float lk = tr.lamr[k];
+        top += lk;
+        S.lam[k] = (lk > 0.f && lk > kDropRel * lam1) ? lk : 0.f;
+        S.order[k] = k;
+      }
+      S.tau = fmaxf(0.f, tr.trace - top);
+    }
+  }
+  __syncthreads();
+
+  // ---- 4. U = Q Y: the reflections in reverse order (warp w, vectors w, w + 8)
+  for (int j = warp; j < r; j += kBuildThreads / 32) {
+    for (int k = n - 3; k >= 0; --k) {
+      const float tau = tr.tau[k];
+      if (tau == 0.f) continue;
+      const int m = n - 1 - k;
+      const float* col = A + (k + 1) * kAS + k;
+      float s = 0.f;
+      float v0 = 0.f, v1 = 0.f;
+      if (lane < m) { v0 = lane == 0 ? 1.f : col[lane * kAS]; s += v0 * U[(k + 1 + lane) * kAS + j]; }
+      if (lane + 32 < m) { v1 = col[(lane + 32) * kAS]; s += v1 * U[(k + 33 + lane) * kAS + j]; }
+      s = tau * group_sum<32>(s);
+      if (lane < m) U[(k + 1 + lane) * kAS + j] -= s * v0;
+      if (lane + 32 < m) U[(k + 33 + lane) * kAS + j] -= s * v1;
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+}
+
+// kTrd: top-r eigenpairs by the tridiagonal solver (trd_top_r) instead of
+// cyclic Jacobi sweeps
+template <int RP, typename T, int PB, bool kTrd>
 __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams prm) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BuildSmem<PB>& S = *reinterpret_cast<BuildSmem<PB>*>(smem_raw);
@@ -339,7 +632,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     const int i = idx / PB, j = idx % PB;
     U[i * kAS + j] = (i == j) ? 1.f : 0.f;
   }
-  {
+  if constexpr (!kTrd) {
     static_assert(sizeof(RoundLabels<PB>) % 4 == 0 && offsetof(BuildSmem<PB>, lp) % 4 == 0 &&
                       offsetof(BuildSmem<PB>, lq) == offsetof(BuildSmem<PB>, lp) + sizeof(S.lp),
                   "round labels are copied as words");
@@ -349,132 +642,150 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   }
   __syncthreads();
 
-  // ---- 3. Jacobi sweeps ------------------------------------------------------
   int sweeps = 0;
-  bool converged = false;
-  for (;;) {
-    // off-diagonal and total Frobenius norms
-    float off = 0.f, tot = 0.f;
-    for (int idx = tid; idx < PB * PB; idx += kBuildThreads) {
-      const int i = idx / PB, j = idx % PB;
-      const float a = A[i * kAS + j];
-      tot += a * a;
-      if (i != j) off += a * a;
-    }
-    off = group_sum<32>(off);
-    tot = group_sum<32>(tot);
-    if (lane == 0) { S.red[2 * warp] = off; S.red[2 * warp + 1] = tot; }
-    __syncthreads();
-    if (tid == 0) {
-      float o = 0.f, t = 0.f;
-      for (int w = 0; w < kBuildThreads / 32; ++w) { o += S.red[2 * w]; t += S.red[2 * w + 1]; }
-      S.flag = (o <= kJacobiTol * kJacobiTol * t) ? 1 : 0;
-    }
-    __syncthreads();
-    if (S.flag) { converged = true; break; }
-    if (sweeps >= prm.max_sweeps) break;
-    ++sweeps;
-    for (int r = 0; r < PB - 1; ++r) {
-      if (tid < NPR) {
-        const int p = S.lp[r][tid], q = S.lq[r][tid];
-        const float app = A[p * kAS + p], aqq = A[q * kAS + q], apq = A[p * kAS + q];
-        float c = 1.f, s = 0.f;
-        if (apq != 0.f) {
-          const float theta = (aqq - app) / (2.f * apq);
-          float t;
-          if (fabsf(theta) > 1e18f) t = 0.5f / theta;
-          else t = (theta >= 0.f ? 1.f : -1.f) / (fabsf(theta) + sqrtf(1.f + theta * theta));
-          c = rsqrtf(1.f + t * t);
-          s = t * c;
-        }
-        S.rot[tid] = make_float4(c, s, __int_as_float(p), __int_as_float(q));
-      }
-      __syncthreads();
-      if (NPR * NPR >= kBuildThreads || tid < NPR * NPR) {
-        // 2 x 2 blocks (K, L): rows (pK, qK), cols (pL, qL); B'' = J_K^T B J_L.
-        // Block tid + 256 m is K = tid % NPR, L = (tid + 256 m) / NPR: the
-        // lanes of a warp run over the pairs K, one column pair L per warp.
-        static_assert(kBuildThreads % NPR == 0, "K is fixed per thread");
-        const int K = tid % NPR;
-        const float4 rK = S.rot[K];
-        const float cK = rK.x, sK = rK.y;
-        const int pK = __float_as_int(rK.z), qK = __float_as_int(rK.w);
-#pragma unroll
-        for (int m = 0; m < (NPR * NPR + kBuildThreads - 1) / kBuildThreads; ++m) {
-          const int L = (tid + kBuildThreads * m) / NPR;
-          const float4 rL = S.rot[L];                 // one broadcast load per warp
-          const float cL = rL.x, sL = rL.y;
-          const int pL = __float_as_int(rL.z), qL = __float_as_int(rL.w);
-          float* a00 = A + pK * kAS + pL;
-          float* a01 = A + pK * kAS + qL;
-          float* a10 = A + qK * kAS + pL;
-          float* a11 = A + qK * kAS + qL;
-          const float b00 = *a00, b01 = *a01, b10 = *a10, b11 = *a11;
-          const float x00 = cK * b00 - sK * b10, x01 = cK * b01 - sK * b11;
-          const float x10 = sK * b00 + cK * b10, x11 = sK * b01 + cK * b11;
-          float n00 = x00 * cL - x01 * sL, n01 = x00 * sL + x01 * cL;
-          float n10 = x10 * cL - x11 * sL, n11 = x10 * sL + x11 * cL;
-          if (K == L) { n01 = 0.f; n10 = 0.f; }
-          *a00 = n00; *a01 = n01; *a10 = n10; *a11 = n11;
-        }
-      }
-      // U <- U J: item tid + 256 m is row i = item % B of pair L = item / B
-      // (the lanes of a warp run over consecutive rows)
-      if (NPR * PB >= kBuildThreads || tid < NPR * PB) {
-#pragma unroll
-        for (int m = 0; m < (NPR * PB + kBuildThreads - 1) / kBuildThreads; ++m) {
-          const int it = tid + kBuildThreads * m;
-          const int i = it % PB, L = it / PB;
-          const float4 rL = S.rot[L];
-          const float cL = rL.x, sL = rL.y;
-          const int pL = __float_as_int(rL.z), qL = __float_as_int(rL.w);
-          const float up = U[i * kAS + pL], uq = U[i * kAS + qL];
-          U[i * kAS + pL] = up * cL - uq * sL;
-          U[i * kAS + qL] = up * sL + uq * cL;
-        }
-      }
-      __syncthreads();
-    }
-  }
-
-  // ---- 4. top-r eigenpairs (warp 0), tau ------------------------------------
+  bool converged = true;
   const int r = prm.rank;
-  if (warp == 0) {
-    // lane holds diagonal entries lane and lane + 32 (those past B count as taken)
-    float v0 = lane < PB ? A[lane * kAS + lane] : 0.f;
-    float v1 = lane + 32 < PB ? A[(lane + 32) * kAS + lane + 32] : 0.f;
-    bool t0 = lane >= PB, t1 = lane + 32 >= PB;
-    float lam1 = 0.f;
-    for (int k = 0; k < r; ++k) {
-      // candidate of this lane: larger value, ties -> lower index
-      float bv = -INFINITY;
-      int bi = 1 << 30;
-      if (!t0) { bv = v0; bi = lane; }
-      if (!t1 && (v1 > bv)) { bv = v1; bi = lane + 32; }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, o);
-        const int oi = __shfl_xor_sync(kFull, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+  if constexpr (kTrd) {
+    trd_top_r<PB>(S, r);
+  } else {
+    converged = false;
+    // ---- 3. Jacobi sweeps ------------------------------------------------------
+    for (;;) {
+      // off-diagonal and total Frobenius norms
+      float off = 0.f, tot = 0.f;
+      for (int idx = tid; idx < PB * PB; idx += kBuildThreads) {
+        const int i = idx / PB, j = idx % PB;
+        const float a = A[i * kAS + j];
+        tot += a * a;
+        if (i != j) off += a * a;
       }
-      if (bi == lane) t0 = true;
-      if (bi == lane + 32) t1 = true;
-      if (k == 0) lam1 = bv;
-      if (lane == 0) {
-        const bool keep = bv > 0.f && bv > kDropRel * lam1;
-        S.lam[k] = keep ? bv : 0.f;
-        S.order[k] = bi;
+      off = group_sum<32>(off);
+      tot = group_sum<32>(tot);
+      if (lane == 0) { S.red[2 * warp] = off; S.red[2 * warp + 1] = tot; }
+      __syncthreads();
+      if (tid == 0) {
+        float o = 0.f, t = 0.f;
+        for (int w = 0; w < kBuildThreads / 32; ++w) { o += S.red[2 * w]; t += S.red[2 * w + 1]; }
+        S.flag = (o <= kJacobiTol * kJacobiTol * t) ? 1 : 0;
+      }
+      __syncthreads();
+      if (S.flag) { converged = true; break; }
+      if (sweeps >= prm.max_sweeps) break;
+      ++sweeps;
+      for (int r = 0; r < PB - 1; ++r) {
+        if (tid < NPR) {
+          const int p = S.lp[r][tid], q = S.lq[r][tid];
+          const float app = A[p * kAS + p], aqq = A[q * kAS + q], apq = A[p * kAS + q];
+          float c = 1.f, s = 0.f;
+          if (apq != 0.f) {
+            const float theta = (aqq - app) / (2.f * apq);
+            float t;
+            if (fabsf(theta) > 1e18f) t = 0.5f / theta;
+            else t = (theta >= 0.f ? 1.f : -1.f) / (fabsf(theta) + sqrtf(1.f + theta * theta));
+            c = rsqrtf(1.f + t * t);
+            s = t * c;
+          }
+          S.rot[tid] = make_float4(c, s, __int_as_float(p), __int_as_float(q));
+        }
+        __syncthreads();
+        if (NPR * NPR >= kBuildThreads || tid < NPR * NPR) {
+          // 2 x 2 blocks (K, L): rows (pK, qK), cols (pL, qL); B'' = J_K^T B J_L.
+          // Block tid + 256 m is K = tid % NPR, L = (tid + 256 m) / NPR: the
+          // lanes of a warp run over the pairs K, one column pair L per warp.
+          static_assert(kBuildThreads % NPR == 0, "K is fixed per thread");
+          const int K = tid % NPR;
+          const float4 rK = S.rot[K];
+          const float cK = rK.x, sK = rK.y;
+          const int pK = __float_as_int(rK.z), qK = __float_as_int(rK.w);
+  #pragma unroll
+          for (int m = 0; m < (NPR * NPR + kBuildThreads - 1) / kBuildThreads; ++m) {
+            const int L = (tid + kBuildThreads * m) / NPR;
+            const float4 rL = S.rot[L];                 // one broadcast load per warp
+            const float cL = rL.x, sL = rL.y;
+            const int pL = __float_as_int(rL.z), qL = __float_as_int(rL.w);
+            float* a00 = A + pK * kAS + pL;
+            float* a01 = A + pK * kAS + qL;
+            float* a10 = A + qK * kAS + pL;
+            float* a11 = A + qK * kAS + qL;
+            const float b00 = *a00, b01 = *a01, b10 = *a10, b11 = *a11;
+            const float x00 = cK * b00 - sK * b10, x01 = cK * b01 - sK * b11;
+            const float x10 = sK * b00 + cK * b10, x11 = sK * b01 + cK * b11;
+            float n00 = x00 * cL - x01 * sL, n01 = x00 * sL + x01 * cL;
+            float n10 = x10 * cL - x11 * sL, n11 = x10 * sL + x11 * cL;
+            if (K == L) { n01 = 0.f; n10 = 0.f; }
+            *a00 = n00; *a01 = n01; *a10 = n10; *a11 = n11;
+          }
+        }
+        // U <- U J: item tid + 256 m is row i = item % B of pair L = item / B
+        // (the lanes of a warp run over consecutive rows)
+        if (NPR * PB >= kBuildThreads || tid < NPR * PB) {
+  #pragma unroll
+          for (int m = 0; m < (NPR * PB + kBuildThreads - 1) / kBuildThreads; ++m) {
+            const int it = tid + kBuildThreads * m;
+            const int i = it % PB, L = it / PB;
+            const float4 rL = S.rot[L];
+            const float cL = rL.x, sL = rL.y;
+            const int pL = __float_as_int(rL.z), qL = __float_as_int(rL.w);
+            const float up = U[i * kAS + pL], uq = U[i * kAS + qL];
+            U[i * kAS + pL] = up * cL - uq * sL;
+            U[i * kAS + qL] = up * sL + uq * cL;
+          }
+        }
+        __syncthreads();
       }
     }
-    float rest = (t0 ? 0.f : fmaxf(v0, 0.f)) + (t1 ? 0.f : fmaxf(v1, 0.f));
-    rest = group_sum<32>(rest);
-    if (lane == 0) S.tau = rest;
+
+    // ---- 4. top-r eigenpairs (warp 0), tau ------------------------------------
+    if (warp == 0) {
+      // lane holds diagonal entries lane and lane + 32 (those past B count as taken)
+      float v0 = lane < PB ? A[lane * kAS + lane] : 0.f;
+      float v1 = lane + 32 < PB ? A[(lane + 32) * kAS + lane + 32] : 0.f;
+      bool t0 = lane >= PB, t1 = lane + 32 >= PB;
+      float lam1 = 0.f;
+      for (int k = 0; k < r; ++k) {
+        // candidate of this lane: larger value, ties -> lower index
+        float bv = -INFINITY;
+        int bi = 1 << 30;
+        if (!t0) { bv = v0; bi = lane; }
+        if (!t1 && (v1 > bv)) { bv = v1; bi = lane + 32; }
+  #pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          const float ov = __shfl_xor_sync(kFull, bv, o);
+          const int oi = __shfl_xor_sync(kFull, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (bi == lane) t0 = true;
+        if (bi == lane + 32) t1 = true;
+        if (k == 0) lam1 = bv;
+        if (lane == 0) {
+          const bool keep = bv > 0.f && bv > kDropRel * lam1;
+          S.lam[k] = keep ? bv : 0.f;
+          S.order[k] = bi;
+        }
+      }
+      float rest = (t0 ? 0.f : fmaxf(v0, 0.f)) + (t1 ? 0.f : fmaxf(v1, 0.f));
+      rest = group_sum<32>(rest);
+      if (lane == 0) S.tau = rest;
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- 5. record: W[0] = mu, W[1+k] = v_k, C[c][i][e] = u_ik sigma_k ----------
+  // The basis V = D^T U_r S_r^-1 re-forms D from the key page: at B = 64 the
+  // page is first brought back into the dead A (one coalesced round of loads
+  // instead of one dependent load per token and dimension); at B = 16 it is
+  // read where it is.
+  const __nv_bfloat16* kp = prm.k_cache + (size_t(blk) * prm.n_kv_heads + h) * (PB * kHeadDim);
+  if constexpr (PB == 64) {
+    static_assert(PB * kHeadDim * 2 <= PB * BuildSmem<PB>::AS * 4, "the key page fits in A");
+    uint4* dst = reinterpret_cast<uint4*>(A);
+#pragma unroll
+    for (int e = 0; e < PB / 16; ++e) dst[tid + kBuildThreads * e] = src[tid + kBuildThreads * e];
+    __syncthreads();
+    kp = reinterpret_cast<const __nv_bfloat16*>(A);
+  }
   if constexpr (std::is_same_v<T, I4Rec>) {
-    write_i4_record<RP, PB>(S, prm, blk, h, r);
+    write_i4_record<RP, PB>(S, prm, blk, h, r, kp);
   } else {
     T* rec = reinterpret_cast<T*>(static_cast<unsigned char*>(prm.summaries) +
                                   (size_t(blk) * prm.n_kv_heads + h) * prm.rec_bytes);
@@ -483,17 +794,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
       const float mu_t = S.mu[t];
       st_elem(rec + t, mu_t);
       // D re-formed from the key page as step 1 formed it (A and U hold its space)
-      const __nv_bfloat16* kp = prm.k_cache + (size_t(blk) * prm.n_kv_heads + h) * (PB * kHeadDim);
       float v[RP];
-#pragma unroll
-      for (int k = 0; k < RP; ++k) v[k] = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < PB; ++i) {
-        const float dit = __bfloat162float(kp[i * kHeadDim + t]) - mu_t;
-#pragma unroll
-        for (int k = 0; k < RP; ++k)
-          if (k < r) v[k] += dit * U[i * kAS + S.order[k]];
-      }
+      basis_column_sums<RP, PB, kAS>(S, kp, t, mu_t, r, v);
 #pragma unroll
       for (int k = 0; k < RP; ++k) {
         const float lam = k < r ? S.lam[k] : 0.f;
@@ -518,7 +820,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
 template <int RP, typename T, int PB>
 int launch_t(const BuildParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(BuildSmem<PB>);
-  auto kern = build_kernel<RP, T, PB>;
+  auto kern = (PB == 64 && p.use_trd) ? build_kernel<RP, T, PB, PB == 64>
+                                      : build_kernel<RP, T, PB, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return LOCKS_ERR_CUDA;

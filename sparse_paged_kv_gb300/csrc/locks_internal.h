@@ -80,6 +80,7 @@ struct BuildParams {
   size_t rec_bytes;
   int n_blocks, n_kv_heads, num_blocks, rank, max_sweeps;
   int skip_negative;             // a negative block id means "no page": skipped, not flagged
+  int use_trd;                   // B = 64: tridiagonal top-r solver instead of Jacobi sweeps
 };
 
 struct AppendParams {

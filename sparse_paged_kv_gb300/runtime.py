@@ -179,7 +179,12 @@ class DecodeLoop:
     alternate, so a step's append never overwrites the list the previous
     step's build may still be reading."""
 
-    def __init__(self, layer: LocksLayer):
+    def __init__(self, layer: LocksLayer, host_lengths=None):
+        """host_lengths: optional int array of the sequences' current lengths
+        as the caller tracks them (an engine knows them: it allocates a block
+        for each page a sequence starts).  With them, a step in which no
+        sequence completes a page launches no build; which blocks are built
+        is still decided on the device, from the `completed` list."""
         import torch
         self.torch = torch
         self.layer = layer
@@ -189,6 +194,7 @@ class DecodeLoop:
         self.appended = torch.cuda.Event()
         self.built = None             # event: the previous step's build is done
         self.steps = 0
+        self.host_lengths = None if host_lengths is None else np.array(host_lengths, dtype=np.int64)
 
     def step(self, k_new, v_new, page_lse=None, page_share=None):
         torch = self.torch
@@ -196,11 +202,17 @@ class DecodeLoop:
         cur = torch.cuda.current_stream(L.device)
         done = self.completed[self.steps & 1]
         L.append(k_new, v_new, completed=done, stream=cur)
-        self.appended.record(cur)
-        self.side.wait_event(self.appended)
-        L.build_completed(done, stream=self.side)
-        built = torch.cuda.Event()
-        built.record(self.side)
+        crosses = True
+        if self.host_lengths is not None:
+            crosses = bool(((self.host_lengths + 1) % L.cfg.page_size == 0).any())
+            self.host_lengths += 1
+        built = None
+        if crosses:
+            self.appended.record(cur)
+            self.side.wait_event(self.appended)
+            L.build_completed(done, stream=self.side)
+            built = torch.cuda.Event()
+            built.record(self.side)
         if self.built is not None:
             cur.wait_event(self.built)
         self.built = built

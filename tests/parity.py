@@ -276,13 +276,16 @@ def record_error(layer, inputs, b: int, h: int, fp64) -> float:
     return err
 
 
-def run_case(inputs, units=None, dense=True, check_build=True, summary_dtype=0):
+def run_case(inputs, units=None, dense=True, check_build=True, summary_dtype=0, max_sweeps=0):
     """Build, select, sparse- and dense-decode on the GPU; compare the given
     units (default: all) with the oracle.  Returns (report, layer, snapshot).
 
     summary_dtype 1 (bf16 records) or 2 (quantised records): the build is
     measured, not gated (report.max_record_err), and selection/scores are
-    gated against the oracle scoring the GPU-stored records."""
+    gated against the oracle scoring the GPU-stored records.
+
+    max_sweeps > 0 builds with the Jacobi solver and that sweep cap (at page
+    size 64 the default is the tridiagonal solver)."""
     import torch
     from sparse_paged_kv_gb300 import runtime
     w = inputs.workload
@@ -291,7 +294,7 @@ def run_case(inputs, units=None, dense=True, check_build=True, summary_dtype=0):
     ids_t = torch.from_numpy(ids).cuda()
     tail = torch.full((max(1, len(ids)), w.n_kv_heads), float("nan"), device="cuda")
     bstat = torch.zeros((max(1, len(ids)), w.n_kv_heads), dtype=torch.int32, device="cuda")
-    layer.build(ids_t, tail_energy=tail, status=bstat)
+    layer.build(ids_t, tail_energy=tail, status=bstat, max_sweeps=max_sweeps)
     page_lse = layer.alloc_page_lse()
     page_share = layer.alloc_page_share()
     layer.select(page_lse=page_lse, page_share=page_share)

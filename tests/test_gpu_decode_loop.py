@@ -42,8 +42,9 @@ def _bf16(torch, a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
 
 
-@pytest.mark.parametrize("wl", [LOOP, LOOP16], ids=["B64", "B16"])
-def test_decode_loop_with_page_crossings(wl):
+@pytest.mark.parametrize("wl,host_lengths", [(LOOP, False), (LOOP16, False), (LOOP, True)],
+                         ids=["B64", "B16", "B64-host-lengths"])
+def test_decode_loop_with_page_crossings(wl, host_lengths):
     import torch
     from sparse_paged_kv_gb300 import runtime
     inputs = W.generate(wl)
@@ -61,7 +62,7 @@ def test_decode_loop_with_page_crossings(wl):
         for j in range(-(-t // B), -(-(t + STEPS) // B)):
             bt_host[b, j] = free.pop(0)
     layer.block_table.copy_(torch.from_numpy(bt_host).cuda())
-    loop = runtime.DecodeLoop(layer)
+    loop = runtime.DecodeLoop(layer, host_lengths=sl_host if host_lengths else None)
     rng = np.random.default_rng(4242)
     page_lse, page_share = layer.alloc_page_lse(), layer.alloc_page_share()
     crossings, scored_new = 0, 0

@@ -80,9 +80,21 @@ def test_parity(name):
     rep, layer, snap = P.run_case(inputs)
     rep.check()
     assert rep.units == CASES[name].batch * CASES[name].n_kv_heads
-    print(f"{name}: lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} dense "
+    print(f"{name}: e_rec*gap {rep.max_recon_gap:.2e} lse {rep.max_lse_err:.2e} out {rep.max_out_err:.2e} dense "
           f"{rep.max_dense_err:.2e} recon {rep.max_recon_rel:.2e} sigma {rep.max_sigma_rel:.2e} "
           f"degenerate {rep.degenerate} ties {rep.tie_diffs}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "rank3", "rank16", "multichunk", "batch_heads"])
+def test_parity_jacobi_solver(name):
+    """The Jacobi solver, which a sweep cap selects at page size 64, against
+    the same oracle gates as the default tridiagonal solver."""
+    inputs = W.generate(CASES[name])
+    rep, layer, snap = P.run_case(inputs, max_sweeps=20)
+    rep.check()
+    assert np.all(snap["build_sweeps"] >= 1)
+    print(f"jacobi {name}: recon {rep.max_recon_rel:.2e} (e_rec*gap {rep.max_recon_gap:.2e}) "
+          f"sigma {rep.max_sigma_rel:.2e} lse {rep.max_lse_err:.2e}")
 
 
 BF16_CASES = ["tiny", "ragged", "group8", "rank16", "multichunk", "slices3", "k40", "b16",
