@@ -607,13 +607,20 @@ __global__ void __launch_bounds__(kSelThreads, (!std::is_same_v<T, I4Rec> &&
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
 
-  // write the per-(warp, unit) partials of every unit this CTA touched
-  for (int t = tid; t < kSelWarps * (u_hi - u_lo + 1) * G; t += kSelThreads) {
-    const int g = t % G, w = (t / G) % kSelWarps, us = t / (G * kSelWarps);
+  // merge the warps' partials of every unit this CTA touched and write one
+  // (max, sum) pair per (CTA, unit, head): the finalize then reads a quarter
+  // as many segments
+  for (int t = tid; t < (u_hi - u_lo + 1) * G; t += kSelThreads) {
+    const int g = t % G, us = t / G;
     const int u = u_lo + us;
+    float m = -INFINITY, s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w) {
+      const float2 v = upart[(w * kUnitSlots + us) * G + g];
+      lse_merge(m, s, v.x, v.y);
+    }
     const int i_first = int((long(u) * p.mc) / p.per_cta);
-    const int seg = (int(blockIdx.x) - i_first) * kSelWarps + w;
-    p.ws_part[(size_t(u) * p.nseg_max + seg) * G + g] = upart[(w * kUnitSlots + us) * G + g];
+    p.ws_part[(size_t(u) * p.nseg_max + (int(blockIdx.x) - i_first)) * G + g] = make_float2(m, s);
   }
 }
 

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   {
     const int i_first = int((long(u) * p.mc) / p.per_cta);
     const int i_last = int((long(u + 1) * p.mc - 1) / p.per_cta);
-    const int nseg = (i_last - i_first + 1) * 4;
+    const int nseg = i_last - i_first + 1;    // one partial per score CTA
     const bool wide = nseg > 128;
     const int stride = wide ? kFinThreads : 32, first = wide ? tid : lane;
     float m[G], s[G];
@@ -265,7 +265,7 @@ SelectGeom select_geometry(int units, int max_pages, int G, int k, int ctas_per_
   if (per > cap) per = cap & ~1L;
   g.per_cta = int(per);
   g.n_score_ctas = int(total > 0 ? (total + per - 1) / per : 1);
-  g.nseg_max = ((g.mc + g.per_cta - 1) / g.per_cta + 1) * kSelWarps;
+  g.nseg_max = (g.mc + g.per_cta - 1) / g.per_cta + 1;
   g.slice = kMaxSlice;
   g.nslices_max = (g.mc + g.slice - 1) / g.slice;
   if (g.nslices_max < 1) g.nslices_max = 1;
