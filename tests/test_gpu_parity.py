@@ -41,6 +41,14 @@ CASES = {
     "group8_k40_slices3": TINY.with_(n_q_heads=16, n_kv_heads=2, context=64 * 4200 + 11,
                                      budget_tokens=64 * 40, seed=2017),
     "group1_slices2": TINY.with_(n_q_heads=2, n_kv_heads=2, context=64 * 2600 + 5, seed=2018),
+    # more than 16384 candidates: nine slices, the last holding 6 candidates
+    # (246 winners merged by direct ranking), and seventeen at B = 16 with
+    # k - 2 > 32 (over 256 winners: the merge takes the bounded top-k)
+    "wide_slices2": TINY.with_(n_q_heads=4, n_kv_heads=1, context=64 * 16391 + 7,
+                               global_rank=16, seed=2050),
+    "b16_wide_slices3_k40": TINY.with_(page_size=16, n_q_heads=4, n_kv_heads=1,
+                                       context=16 * 33000 + 9, budget_tokens=16 * 40,
+                                       global_rank=16, seed=2051),
     # page size 16 (four pages per decode stage)
     "b16": TINY.with_(page_size=16, seed=2020),
     "b16_ragged": TINY.with_(page_size=16, batch=5, seq_lens=(4096 + 7, 200, 16 * 33, 9, 0),
@@ -117,7 +125,8 @@ def test_parity_bf16_records(name):
 
 I4_CASES = ["tiny", "ragged", "group1", "group2", "group8", "rank16", "rank3", "multichunk",
             "slices3", "k40", "b16", "b16_ragged", "b16_rank15", "cluster_merge", "batch_heads",
-            "group8_k40_slices3", "heads16", "ragged_8heads", "b16_gqa4_k128"]
+            "group8_k40_slices3", "heads16", "ragged_8heads", "b16_gqa4_k128",
+            "b16_wide_slices3_k40"]
 
 
 @pytest.mark.parametrize("name", I4_CASES)
@@ -266,16 +275,17 @@ def test_graph_replay_matches_eager_and_oracle():
     assert int(layer.status.cpu()[0]) == 0
 
 
-@pytest.mark.parametrize("summary_dtype", [0, 2])
-@pytest.mark.parametrize("context", [64 * 1500 + 9, 64 * 4200 + 11])
+@pytest.mark.parametrize("summary_dtype,context", [
+    (0, 64 * 1500 + 9), (2, 64 * 1500 + 9), (0, 64 * 4200 + 11), (2, 64 * 4200 + 11),
+    (0, 64 * 16391 + 7)])
 def test_equal_shares_select_the_smallest_pages(context, summary_dtype):
     """With zero queries every logit is 0, so every complete page has the same
     s_hat and the same share: the selection is then decided by the tie rule
     alone (between equal shares the smaller page), i.e. pages 1 .. k-2 besides
-    the forced ones.  1499 candidates in one slice, or three slices of up to
-    2048, leave more equal keys above the top-K's lower bound than its ranking
-    buffer holds, so the bit-by-bit search decides; the slices' winners are
-    then merged through the ranking path."""
+    the forced ones.  1499 candidates in one slice, or three or nine slices
+    of up to 2048, leave more equal keys above the top-K's lower bound than
+    its ranking buffer holds, so the bit-by-bit search decides; the slices'
+    winners are then merged through the ranking path."""
     import torch
     from sparse_paged_kv_gb300 import runtime
     w = TINY.with_(context=context, seed=2040)
