@@ -19,6 +19,9 @@ constexpr int kAppendThreads = 256;
 constexpr int kRowWords = kHeadDim * 2 / 16;   // 16-byte words of one bf16 row
 
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
+  // the selection's score kernel that follows may start launching at once:
+  // it reads nothing before its own wait for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.x;
   const int B = p.page_size;
   __shared__ int s_blk, s_pos;

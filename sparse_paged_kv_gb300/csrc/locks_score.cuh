@@ -488,6 +488,10 @@ __global__ void __launch_bounds__(kSelThreads, (!std::is_same_v<T, I4Rec> &&
     for (int s = 0; s < STAGES; ++s) mbar_init(mybar + s, 1);
     mbar_fence_init();
   }
+  // launched as a programmatic dependent of the previous kernel in the stream
+  // (in a decode loop, the append of the step's token): everything below
+  // reads what that kernel may write
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int t = tid; t < n_f; t += kSelThreads) {
     const long f = f_lo + t;
     const int u = int(f / p.mc), idx = int(f % p.mc);
@@ -640,8 +644,17 @@ int launch_score_t(const SelectParams& p, int n_ctas, cudaStream_t stream) {
   if (cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return LOCKS_ERR_CUDA;
-  sk<<<n_ctas, kSelThreads, smem, stream>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(n_ctas);
+  lc.blockDim = dim3(kSelThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, sk, p) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
 }
 
 template <typename T, int PB>
