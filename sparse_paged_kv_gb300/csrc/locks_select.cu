@@ -19,8 +19,9 @@
 //   forms the reconstructed logits of tokens l, l+16, l+32, l+48 for every
 //   head and reduces them by log-sum-exp (transposed max and sum).
 // For the quantised record the whole warp scores the pair with f16 mma (see
-// score_pair_i4).  The kernel writes s_hat per (page, head) and, per warp and
-// unit, the running (max, sum) log-sum-exp of its s_hat values.
+// score_pair_i4).  The kernel writes s_hat per (page, head) and, per CTA and
+// unit, the (max, sum) log-sum-exp of its s_hat values (its warps' running
+// pairs merged in the CTA).
 //
 // finalize_kernel: CTA (slice, unit) merges the unit's partials into log Z_g
 // (each warp by itself), forms the averaged shares m_bar_j of its slice of
