@@ -40,8 +40,38 @@ namespace locks {
 
 namespace {
 
+// distributed shared memory (the unit's slices as one thread-block cluster)
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint2 ld_cluster_u2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+// every thread of every CTA of the cluster; shared-memory writes before it are
+// visible to the cluster's loads after it
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release;\n"
+      "barrier.cluster.wait.acquire;" ::: "memory");
+}
 
-template <int G>
+// CL: the unit's slices form one thread-block cluster (2 to 8 slices) and
+// merge their winners through distributed shared memory; otherwise the last
+// slice to finish (atomic ticket) merges them from global memory.
+template <int G, bool CL>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   // launched as a programmatic dependent of the score kernel: what it reads
@@ -63,15 +93,75 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
   int* pages = reinterpret_cast<int*>(keys + p.fin_cap);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (sl >= nsl) return;
   const int k = p.k, K = k - 2;
   int32_t* out = p.selected + size_t(u) * k;
+  const bool select = n > k && K > 0;
 
   __shared__ TopkScratch ts;
   __shared__ int s_is_last;
+  __shared__ uint2 s_win[256];               // clustered merge: this slice's winners
+  __shared__ int s_flag[256];
+  __shared__ int s_ng, s_off;
+  // ---- clustered merge (every CTA of the cluster, n_own winners here) -------
+  // Each slice copies all slices' winners (in slice order, so page order) into
+  // its own shared memory and ranks its own against them, several threads to
+  // a winner; those of rank < K are selected.  A winner's place in the output
+  // is the number of selected winners of the slices before it plus its place
+  // among its own slice's, so the slices exchange their counts once more.
+  // Three cluster barriers: winners written, counts written, counts read.
+  auto cluster_merge = [&](int n_own) {
+    cluster_barrier();
+    int x = 0;
+    if (n_own > 0) {                         // uniform in the CTA
+      const int m_all = (nsl - 1) * K + min(K, n_cand - (nsl - 1) * p.slice);
+      const uint32_t base = smem_u32(s_win);
+      for (int i = tid; i < m_all; i += kFinThreads) {
+        const int s2 = i / K, e2 = i - s2 * K;
+        const uint2 e = ld_cluster_u2(cluster_addr(base + 8u * uint32_t(e2), s2));
+        keys[i] = e.x;
+        pages[i] = int(e.y);
+      }
+      __syncthreads();
+      const int tpc = n_own <= 32 ? 8 : n_own <= 64 ? 4 : n_own <= 128 ? 2 : 1;
+      const int c = tid / tpc, q = tid - c * tpc;
+      int r = 0;
+      if (c < n_own) {
+        const int ge = sl * K + c;
+        const uint32_t mine = keys[ge];
+        for (int j = q; j < m_all; j += tpc) {
+          const uint32_t o = keys[j];
+          r += (o > mine || (o == mine && j < ge)) ? 1 : 0;
+        }
+      }
+      for (int o = tpc >> 1; o >= 1; o >>= 1) r += __shfl_xor_sync(kFull, r, o);
+      if (c < n_own && q == 0) s_flag[c] = r < K ? 1 : 0;
+      __syncthreads();
+      x = tid < n_own ? s_flag[tid] : 0;
+    }
+    const int pos = block_excl_scan(x, ts.scan[0]);
+    if (tid == kFinThreads - 1) s_ng = pos + x;
+    cluster_barrier();
+    if (tid < 32) {
+      int v = lane < sl ? ld_cluster_s32(cluster_addr(smem_u32(&s_ng), lane)) : 0;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+      if (lane == 0) s_off = v;
+    }
+    __syncthreads();
+    if (x) out[1 + s_off + pos] = pages[sl * K + tid];
+    if (sl == 0 && tid == 0) { out[0] = 0; out[k - 1] = n - 1; }
+    cluster_barrier();
+  };
+  if (sl >= nsl) {
+    // in a cluster the slices past the unit's candidates still meet at its
+    // barriers (the condition is uniform in the cluster: one unit)
+    if constexpr (CL) {
+      if (select && nsl > 1) cluster_merge(0);
+    }
+    return;
+  }
   const float* ws_s = p.ws_scores + size_t(u) * p.max_pages * G;
   const int c_lo = sl * p.slice, c_n = min(n_cand, c_lo + p.slice) - c_lo;   // <= slice
-  const bool select = n > k && K > 0;
   // the slice's scores go out first: they do not depend on log Z
   constexpr int kPer = kMaxSlice / kFinThreads;
   float sv[kPer][G];
@@ -198,6 +288,12 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
     if (tid == 0) { out[0] = 0; out[k - 1] = n - 1; }
     return;
   }
+  if constexpr (CL) {
+    uint2* win = s_win;
+    topk(c_n, K, [=](int i, int pos) { win[pos] = make_uint2(keys[i], uint32_t(1 + c_lo + i)); });
+    cluster_merge(min(K, c_n));
+    return;
+  }
   uint2* cand = p.ws_cand + (size_t(u) * p.nslices_max + sl) * p.cand_per_slice;
   topk(c_n, K, [=](int i, int pos) { cand[pos] = make_uint2(keys[i], uint32_t(1 + c_lo + i)); });
 
@@ -226,8 +322,10 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const SelectParam
 template <int G>
 int launch_finalize(const SelectParams& p, int n_slices, cudaStream_t stream) {
   const size_t fsmem = size_t(p.fin_cap) * 8;
-  if (fsmem + sizeof(TopkScratch) + 1024 > kMaxDynSmem) return LOCKS_ERR_UNSUPPORTED;
-  auto fk = finalize_kernel<G>;
+  if (fsmem + sizeof(TopkScratch) + 6144 > kMaxDynSmem) return LOCKS_ERR_UNSUPPORTED;
+  // 2 to 8 slices a unit (portable cluster sizes): one cluster per unit
+  const bool cl = n_slices >= 2 && n_slices <= 8;
+  auto fk = cl ? finalize_kernel<G, true> : finalize_kernel<G, false>;
   if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, int(fsmem)) !=
       cudaSuccess)
     return LOCKS_ERR_CUDA;
@@ -236,11 +334,15 @@ int launch_finalize(const SelectParams& p, int n_slices, cudaStream_t stream) {
   lc.blockDim = dim3(kFinThreads);
   lc.dynamicSmemBytes = fsmem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = n_slices;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = cl ? 2 : 1;
   return cudaLaunchKernelEx(&lc, fk, p) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
 }
 
