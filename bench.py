@@ -457,6 +457,13 @@ def l2_policy(torch, w, rec_bytes: int):
     return True, FLUSH_NOTE
 
 
+def gpu_spin(torch, stream, ms: float = 5.0):
+    """Keep the device busy for about ms milliseconds (torch's spin kernel,
+    at the 2.07 GHz SM clock) on `stream`."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(ms * 2.07e6))
+
+
 class Timer:
     """Event-timed loops on one stream, with (flush=True) an L2 flush before
     every iteration: write 256 MiB (> the 129 MB L2), then read another
@@ -513,6 +520,10 @@ class Timer:
         torch.cuda.synchronize()
         ctx = region if region is not None else _Null()
         with ctx:
+            # a spin on the device before the region, so that the host has
+            # queued the region's launches by the time it starts: the region
+            # then holds device time only, not the host's first launches
+            gpu_spin(torch, self.stream)
             e0.record(self.stream)
             for _ in range(n_steps):
                 fn(None)
@@ -729,6 +740,7 @@ def measure_record(layer, inputs, timer, K, Wm, sampler, tag, full, args, world,
 
             def erun(ev):
                 if ev:
+                    gpu_spin(torch, stream)               # host launches queue up first
                     ev[0].record(stream)
                     up.wait_event(ev[0])                  # the first copy is inside the region
                 pipelined(K)
@@ -769,6 +781,7 @@ def measure_decode_loop(layer, w, sampler, tag, reps=5):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def plain():
+        gpu_spin(torch, stream)
         e0.record(stream)
         for _ in range(B):
             layer.select()
@@ -783,6 +796,7 @@ def measure_decode_loop(layer, w, sampler, tag, reps=5):
         layer.seq_lens.copy_(lens0 - B)
         loop = runtime.DecodeLoop(layer, host_lengths=host_lens - B)
         torch.cuda.synchronize()
+        gpu_spin(torch, stream)
         e0.record(stream)
         for s in range(B):
             loop.step(rows[s, 0], rows[s, 1])
