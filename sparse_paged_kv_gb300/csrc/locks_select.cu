@@ -3,7 +3,8 @@
 // "Locks: Page-Local Compact Key Summaries for Efficient Long-Context
 // Decoding", section 4 ("Score") and Cor. 3.
 //
-// Two kernels, the second launched as a programmatic dependent of the first:
+// Two kernels, the second launched as a programmatic dependent of the first
+// (and the sparse decode as one of the second):
 //
 // score_kernel: the candidate pages of every (sequence b, KV
 // head h) "unit" are laid end to end (mc slots per unit) and every CTA takes
@@ -24,13 +25,19 @@
 // pairs merged in the CTA).
 //
 // finalize_kernel: CTA (slice, unit) merges the unit's partials into log Z_g
-// (each warp by itself), forms the averaged shares m_bar_j of its slice of
-// candidates and finds the slice's top-(k-2) (block_topk: the (k-2)-th largest
-// per-thread maximum bounds the answer from below, the few shares at or above
-// it are ranked against one another; between equal shares the smaller page
-// wins); the winners are written in page order by one block scan.  The last slice of the unit (atomic ticket, no
-// waiting) selects among the slices' winners the same way and writes the
-// forced pages and the winners in ascending page order.
+// (each warp by itself), forms the averaged shares m_bar_j of its slice of up
+// to 2048 candidates and finds the slice's top-(k-2) (block_topk: a per-warp
+// order statistic of the per-thread maxima bounds the answer from below, the
+// few shares at or above it are ranked against one another; between equal
+// shares the smaller page wins); one block scan writes the winners in page
+// order.  A unit of 2 to 8 slices is one thread-block cluster whose CTAs merge
+// their winners through distributed shared memory; with more slices the last
+// one to finish (atomic ticket, no waiting) selects among the slices' winners.
+// Either way the forced pages and the winners are written in ascending page
+// order.
+//
+// The score kernel itself is launched as a programmatic dependent of whatever
+// precedes it on the stream, and waits for it before reading anything.
 #include <mutex>
 
 #include "locks_score.cuh"
