@@ -601,14 +601,21 @@ int launch_list(DecodeParams p, const CUtensorMap& tk, const CUtensorMap& tv, in
     // equal-length lists: one cluster of at most kMaxClusterSplits splits per
     // unit, each split a whole number of ring stages
     constexpr int PPS = kStageTokens / PB;
-    int pps = std::max(p.pages_per_split, (p.k + kMaxClusterSplits - 1) / kMaxClusterSplits);
+    // Few units (at most 16, as at a million tokens with one sequence): the
+    // decode is a latency chain, and clusters of up to 8 splits of several
+    // pages, merged on chip, end it sooner than a ticketed merge of many
+    // one-page splits (1M: 1 us per step).  More units: only small clusters
+    // (at most kMaxMergeCluster CTAs): in a decode step, which starts while
+    // the selection's kernels still hold SMs, larger clusters were measured to
+    // start late (32 units in clusters of 8: 5 us slower per step than the
+    // ticketed merge of the same 8 splits).
+    const bool few_units = gy <= 16;
+    const int cap = few_units ? 8 : kMaxMergeCluster;
+    const int most = few_units ? 8 : kMaxClusterSplits;
+    int pps = std::max(p.pages_per_split, (p.k + most - 1) / most);
     pps = (pps + PPS - 1) / PPS * PPS;
     const int C = (p.k + pps - 1) / pps;
-    // Only small clusters (at most kMaxMergeCluster CTAs, two SMs): in a decode
-    // step, which starts while the selection's kernels still hold SMs, larger
-    // clusters were measured to start late (32 units in clusters of 8: 5 us
-    // slower per step than the ticketed merge of the same 8 splits).
-    if (C <= kMaxMergeCluster && cluster_capacity<G, PB>(C) > 0) {
+    if (C <= cap && cluster_capacity<G, PB>(C) > 0) {
       p.pages_per_split = pps;
       return launch_g<G, PB>(p, tk, tv, C, gy, true, stream);
     }
