@@ -84,6 +84,18 @@ def _select(lib, c, budget=512, ws_bytes=1 << 30, **over):
                             budget, args["sel"], None, None, args["ws"], ws_bytes, None, None)
 
 
+def test_headline_shape_sizes(lib):
+    """The 1M-token layer (one sequence, 32/8 heads, 16384 pages): the select
+    workspace holds s_hat for every (unit, page, head) plus the partials, the
+    slice winners and the tickets, a few MB; the quantised record is 1456
+    bytes at r = 8, B = 64."""
+    c = cfg(batch=1, n_q_heads=32, n_kv_heads=8, max_pages=16384, num_blocks=16384 + 8)
+    ws = B.select_workspace_bytes(c, 2048)
+    assert 8 * 16384 * 4 * 4 <= ws < 16 * 2 ** 20
+    assert B.decode_workspace_bytes(c, 32) > 0
+    assert B.summary_record_bytes(cfg(summary_dtype=B.LOCKS_SUMMARY_I4)) == 1456
+
+
 def test_select_validation(lib):
     assert _select(lib, cfg(), budget=64) == B.LOCKS_ERR_INVALID_ARG        # k = 1
     assert _select(lib, cfg(), budget=0) == B.LOCKS_ERR_INVALID_ARG
